@@ -1,0 +1,232 @@
+/*
+ * evs.h - replay-free speculative block verification for a hybrid short-FIR /
+ * modal-IIR / causal-attention target, on one GB300 (sm_103a).
+ *
+ * Method: "EvSpark: Lossless Speculative Decoding for Hybrid DNA Foundation Models"
+ * (summary page). Figure 1(c): the target verifies the old anchor plus gamma drafts in
+ * one block forward and a correction becomes the next unconsumed anchor. Figure 1(d):
+ * state returns to the accepted block index k - the readable KV prefix is shortened, the
+ * last L-1 outer-FIR inputs are selected and IIR state s_k is kept - with no target
+ * computation replayed. Interpretation, paragraph 1: one initial-state block forward plus
+ * a common state-slicing protocol (Lemma 2 block-forward contract, Lemma 3 state
+ * restoration, Theorem 1 sequence-level exactness). Acceptance: greedy argmax match, or
+ * rejection sampling with min(1, p/q) and a correction from norm(max(0, p - q))
+ * (ReaDy summary, section 3.1 and appendix D.2).
+ *
+ * Target model (the pages name only the three state classes; this is the reading the
+ * library implements): h = E[x]; per layer xh = h / sqrt(mean(h^2) + 1e-6), then
+ *   FIR-L : v = xh W_in, y_t = sum_{j<L} taps[:, j] * v_{t-j},            h += y W_out
+ *   IIR-N : u = xh W_in, s_t = lam * s_{t-1} + b * u_t (N complex poles),
+ *           y = Re sum_n c_n s_{t,n},                                       h += y W_out
+ *   attn  : q, k, v = xh W_q, W_k, W_v; per head softmax(q K^T / sqrt(dh)) V over the
+ *           readable cache plus the block keys up to the query's position,  h += o W_o
+ * logits = (h / rms(h)) W_head; p = softmax(logits / temperature).
+ *
+ * Conventions
+ *   - Every entry point is asynchronous on the handle's stream unless stated otherwise,
+ *     and never synchronises the device. Pointers marked "device" must be device memory
+ *     (or managed memory) valid until the enqueued work completes.
+ *   - The caller owns every buffer: weights, the workspace and all inputs and outputs.
+ *     The handle stores pointers into them and owns only its host-side struct.
+ *   - Matrices are "out-major": row n is output channel n, its input weights
+ *     contiguous (the transpose of the math convention y = x W).
+ *   - dtype EVS_DTYPE_BF16 stores weights, activations fed to projections, and K/V in
+ *     bfloat16; accumulation, the residual stream, FIR inputs and the complex IIR state
+ *     are fp32. EVS_DTYPE_F32 keeps everything in fp32.
+ *   - Block rows are ordered m = (b * n_cand + c) * (gamma + 1) + i, i = block position
+ *     (0 = anchor, i >= 1 = draft i).
+ *   - Errors found on the host are returned before anything is enqueued. Kernels never
+ *     trap: a condition only the device can see (a KV capacity overflow, k outside
+ *     [0, gamma], a token id out of range) skips or clamps the affected access and sets a
+ *     bit readable through evs_device_flags.
+ */
+#ifndef EVS_H
+#define EVS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct evs_handle evs_handle;
+
+typedef enum {
+    EVS_OK = 0,
+    EVS_ERR_INVALID_ARG = 1, /* null pointer, bad size, unsupported shape            */
+    EVS_ERR_CAPACITY = 2,    /* KV rows would exceed t_max, or workspace too small   */
+    EVS_ERR_STATE = 3,       /* call out of order (slice without a verify before it) */
+    EVS_ERR_CUDA = 4         /* a CUDA runtime call or kernel launch failed          */
+} evs_status;
+
+enum { EVS_LAYER_FIR = 0, EVS_LAYER_IIR = 1, EVS_LAYER_ATTN = 2 };
+enum { EVS_DTYPE_F32 = 0, EVS_DTYPE_BF16 = 1 };
+enum { EVS_MODE_GREEDY = 0, EVS_MODE_SAMPLING = 1 };
+
+/* Bits of the device flag word (evs_device_flags). */
+enum {
+    EVS_FLAG_KV_OVERFLOW = 1u,    /* a write past t_max was skipped                     */
+    EVS_FLAG_BAD_K = 2u,          /* slice saw k outside [0, gamma] or a bad candidate  */
+    EVS_FLAG_EMPTY_RESIDUAL = 4u, /* max(0, p - q) summed to 0 in fp32; p was used      */
+    EVS_FLAG_BAD_TOKEN = 8u       /* a token id outside [0, vocab) was clamped          */
+};
+
+#define EVS_MAX_LAYERS 64
+
+typedef struct {
+    int32_t d;                            /* model width (multiple of 64, <= 8192)      */
+    int32_t vocab;                        /* vocabulary (256 * 2^j, 256 .. 4096)        */
+    int32_t n_layers;                     /* 1 .. EVS_MAX_LAYERS                        */
+    int32_t layer_kind[EVS_MAX_LAYERS];   /* EVS_LAYER_*                                */
+    int32_t layer_param[EVS_MAX_LAYERS];  /* FIR taps L (2..16) | IIR poles N (1,2,4,8,16,32)
+                                             | attention heads H (H * head_dim == d)    */
+    int32_t head_dim;                     /* attention head width (16, 32, 64 or 128)   */
+    int32_t gamma;                        /* drafts per block (1..31)                   */
+    int32_t batch;                        /* sequences B (1..64)                        */
+    int32_t n_cand;                       /* candidate blocks C per sequence            */
+    int32_t t_max;                        /* KV capacity per sequence, tokens           */
+    int32_t prefill_chunk;                /* tokens per sequence per prefill pass       */
+    int32_t dtype;                        /* EVS_DTYPE_*                                */
+    int32_t mode;                         /* EVS_MODE_*                                 */
+    float temperature;                    /* p = softmax(logits / temperature), > 0     */
+    float near_tie_tau;                   /* relative threshold of the near-tie flags   */
+} evs_config;
+
+typedef struct {
+    const void* w_in;        /* FIR, IIR: [d][d] out-major, dtype                        */
+    const void* w_out;       /* FIR, IIR: [d][d] out-major, dtype                        */
+    const float* fir_taps;   /* FIR: [d][L] fp32, taps[c][j] multiplies v_{t-j}[c]        */
+    const float* iir_lambda; /* IIR: [d][N][2] fp32 (re, im) poles                         */
+    const float* iir_b;      /* IIR: [d][N][2] fp32 input coefficients                     */
+    const float* iir_c;      /* IIR: [d][N][2] fp32 readout coefficients                   */
+    const void* w_qkv;       /* attn: [3d][d] out-major, dtype; rows q (0..d-1), k, v     */
+    const void* w_o;         /* attn: [d][d] out-major, dtype                              */
+} evs_layer_weights;
+
+typedef struct {
+    const void* embed;                    /* [vocab][d] dtype                            */
+    const void* head;                     /* [vocab][d] out-major dtype                  */
+    evs_layer_weights layer[EVS_MAX_LAYERS];
+} evs_weights;
+
+/* Caller-side view of the decode state, for import / export (checkpoint and resume;
+ * the slicing contract of Figure 1(d) is exactly this state). Pointers are device
+ * memory except kv_len. Arrays are indexed by layer index; entries of other kinds are
+ * ignored. */
+typedef struct {
+    int32_t* kv_len;                        /* host [B] readable KV length per sequence */
+    int32_t t_stride;                       /* rows per (sequence, head) in k and v      */
+    void* k[EVS_MAX_LAYERS];                /* attn: [B][H][t_stride][dh] dtype          */
+    void* v[EVS_MAX_LAYERS];                /* attn: [B][H][t_stride][dh] dtype          */
+    float* fir_tail[EVS_MAX_LAYERS];        /* FIR: [B][L-1][d] fp32, oldest input first */
+    float* iir_state[EVS_MAX_LAYERS];       /* IIR: [B][d][N][2] fp32                    */
+} evs_state_view;
+
+/* Internal buffers exposed read-only for tests and diagnostics (evs_debug_buffer). */
+enum {
+    EVS_BUF_LOGITS = 0,     /* [B*C*(gamma+1)][vocab] fp32, last verify                 */
+    EVS_BUF_FIR_STAGE = 1,  /* layer: [B][C][L-1+gamma+1][d] fp32 = [tail || inputs v]    */
+    EVS_BUF_IIR_RET = 2,    /* layer: [B][C][gamma+1][d][N][2] fp32, s_0..s_gamma         */
+    EVS_BUF_K_CACHE = 3,    /* layer: [B][H][t_max][dh] dtype                             */
+    EVS_BUF_V_CACHE = 4,    /* layer: [B][H][t_max][dh] dtype                             */
+    EVS_BUF_K_SIDE = 5,     /* layer, n_cand > 1: [B][C][H][gamma+1][dh] dtype block keys  */
+    EVS_BUF_V_SIDE = 6,     /* layer, n_cand > 1: [B][C][H][gamma+1][dh] dtype             */
+    EVS_BUF_KV_LEN = 7,     /* [B] int32                                                  */
+    EVS_BUF_FIR_TAIL = 8,   /* layer: [B][L-1][d] fp32                                    */
+    EVS_BUF_IIR_STATE = 9,  /* layer: [B][d][N][2] fp32                                   */
+    EVS_BUF_CAND_K = 10,    /* [B][C] int32 accepted drafts per candidate, last verify    */
+    EVS_BUF_CAND_CORR = 11  /* [B][C] int32 correction per candidate, last verify         */
+};
+
+typedef struct {
+    void* ptr;        /* device pointer into the workspace (do not write)              */
+    size_t bytes;
+} evs_buffer_info;
+
+/* Bytes of device workspace that evs_create needs for this configuration (0 if the
+ * configuration is invalid). Pure host function. */
+size_t evs_workspace_bytes(const evs_config* cfg);
+
+/* Validate the configuration, lay out state and scratch buffers inside the caller's
+ * workspace (device, >= evs_workspace_bytes, 256-byte aligned) and build the handle.
+ * Weights are device pointers in the layouts above and must outlive the handle.
+ * stream is a cudaStream_t (NULL = legacy default stream). The state starts empty
+ * (kv_len = 0, FIR tails and IIR states zero); the zeroing is enqueued on the stream.
+ * Returns EVS_ERR_INVALID_ARG for a bad configuration or pointer, EVS_ERR_CAPACITY if
+ * ws_bytes is too small, EVS_ERR_CUDA if a CUDA call fails. */
+evs_status evs_create(const evs_config* cfg, const evs_weights* weights, void* workspace,
+                      size_t ws_bytes, void* stream, evs_handle** out);
+
+/* Free the host-side handle. Does not touch caller-owned memory. NULL is allowed. */
+void evs_destroy(evs_handle* h);
+
+/* Change the stream later calls enqueue on (a cudaStream_t). */
+evs_status evs_set_stream(evs_handle* h, void* stream);
+
+/* Return the state to empty (kv_len 0, zero FIR tails and IIR states). */
+evs_status evs_reset(evs_handle* h);
+
+/* Consume P prefix tokens per sequence from the current state, prefill_chunk tokens per
+ * pass, committing every pass (no logits are produced). tokens: device int32 [B][P],
+ * ids in [0, vocab). Prefill is excluded from the pages' token benchmarks (Perspective,
+ * paragraph 1). EVS_ERR_CAPACITY if kv_len + P could exceed t_max. */
+evs_status evs_prefill(evs_handle* h, const int32_t* tokens, int32_t P);
+
+/* One block forward plus acceptance (Figure 1(c); Lemma 2).
+ *   tokens   device int32 [B][C][gamma+1]: position 0 is the anchor, 1..gamma drafts.
+ *   anchor   device int32 [B] or NULL: when given, replaces tokens[b][c][0] for every
+ *            candidate (pass the previous round's correction to chain rounds).
+ *   q_probs  device fp32 [B][C][gamma][vocab]: draft distributions (sampling mode; NULL
+ *            in greedy mode).
+ *   uniforms device fp32 [B][C][gamma+1] in [0, 1): u[j] tests draft j+1 by
+ *            u * q(d) < p(d); u[gamma] draws the correction or bonus by inverse CDF over
+ *            ascending ids (sampling mode; NULL in greedy mode).
+ * Outputs (device, written by the enqueued kernels):
+ *   accepted_len [B] int32: k, accepted drafts of the committed candidate (0..gamma).
+ *   correction   [B] int32: next anchor (correction at the first rejection, or bonus).
+ *   best_cand    [B] int32 or NULL: committed candidate (most accepted drafts, lowest
+ *                index on ties); required when n_cand > 1.
+ *   near_tie     [B] uint32 or NULL: 1 when a decision was within near_tie_tau of
+ *                flipping (greedy top-2 logit gap < tau * rms(logits); |u q - p| < tau p;
+ *                u * sum(r) within tau * sum(r) of an inverse-CDF boundary).
+ * Writes the block's K/V rows, FIR inputs and every IIR state s_0..s_gamma into the
+ * workspace for evs_slice_state. State itself is not modified.
+ * EVS_ERR_CAPACITY if kv_len + gamma + 1 could exceed t_max. */
+evs_status evs_verify_block(evs_handle* h, const int32_t* tokens, const int32_t* anchor,
+                            const float* q_probs, const float* uniforms,
+                            int32_t* accepted_len, int32_t* correction, int32_t* best_cand,
+                            uint32_t* near_tie);
+
+/* State slicing at the accepted index (Figure 1(d); Lemma 3), in place, no replay:
+ * kv_len += k + 1 (for n_cand > 1 the chosen candidate's k+1 block K/V rows are first
+ * copied into the cache), FIR tail <- the last L-1 inputs up to block position k, IIR
+ * state <- s_k. accepted_len and best_cand are device int32 [B] (usually the outputs of
+ * the verify; best_cand may be NULL when n_cand == 1). k stays on the device: nothing is
+ * read back. EVS_ERR_STATE if no verify was enqueued since the last slice or prefill. */
+evs_status evs_slice_state(evs_handle* h, const int32_t* accepted_len, const int32_t* best_cand);
+
+/* Copy a caller state into the handle (import) or the handle's state out (export).
+ * Enqueued copies; export writes kv_len to the host view after synchronising the
+ * stream. Import rejects kv_len > t_max or > t_stride with EVS_ERR_CAPACITY. */
+evs_status evs_import_state(evs_handle* h, const evs_state_view* view);
+evs_status evs_export_state(evs_handle* h, const evs_state_view* view);
+
+/* Read-only location of an internal buffer (see EVS_BUF_*); layer is a layer index
+ * where the buffer is per layer. EVS_ERR_INVALID_ARG if the buffer does not exist. */
+evs_status evs_debug_buffer(evs_handle* h, int32_t which, int32_t layer, evs_buffer_info* out);
+
+/* Synchronise the stream and return the device flag word (EVS_FLAG_*); clear it when
+ * clear != 0. */
+evs_status evs_device_flags(evs_handle* h, uint32_t* flags, int32_t clear);
+
+/* Number of kernel launches the last public call enqueued (for accounting). */
+int32_t evs_last_launch_count(evs_handle* h);
+
+/* Static description of a status code. */
+const char* evs_status_str(evs_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EVS_H */

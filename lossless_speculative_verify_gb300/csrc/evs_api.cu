@@ -1,0 +1,463 @@
+// C-ABI entry points: configuration checks, workspace layout, pass orchestration,
+// state import / export. Everything is enqueued on the handle's stream; nothing here
+// synchronises except evs_export_state and evs_device_flags, which say so.
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "evs_internal.h"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+inline int elem_bytes(const evs_config& c) { return c.dtype == EVS_DTYPE_BF16 ? 2 : 4; }
+
+bool valid_config(const evs_config* c) {
+    if (!c) return false;
+    if (c->d < 64 || c->d > 8192 || c->d % 64) return false;
+    if (!(c->vocab == 256 || c->vocab == 512 || c->vocab == 1024 || c->vocab == 2048 || c->vocab == 4096))
+        return false;
+    if (c->n_layers < 1 || c->n_layers > EVS_MAX_LAYERS) return false;
+    if (!(c->head_dim == 16 || c->head_dim == 32 || c->head_dim == 64 || c->head_dim == 128)) return false;
+    for (int i = 0; i < c->n_layers; ++i) {
+        const int k = c->layer_kind[i], p = c->layer_param[i];
+        if (k == EVS_LAYER_FIR) {
+            if (p < 2 || p > 16) return false;
+        } else if (k == EVS_LAYER_IIR) {
+            if (!(p == 1 || p == 2 || p == 4 || p == 8 || p == 16 || p == 32)) return false;
+        } else if (k == EVS_LAYER_ATTN) {
+            if (p < 1 || (long long)p * c->head_dim != c->d) return false;
+        } else {
+            return false;
+        }
+    }
+    if (c->gamma < 1 || c->gamma > 31) return false;
+    if (c->batch < 1 || c->batch > 64 || c->n_cand < 1 || c->n_cand > 16) return false;
+    if ((long long)c->batch * c->n_cand * (c->gamma + 1) > 512) return false;
+    if (c->prefill_chunk < 1 || c->prefill_chunk > 128) return false;
+    if ((long long)c->batch * c->prefill_chunk > 1024) return false;
+    if (c->t_max < 1) return false;
+    if (c->dtype != EVS_DTYPE_F32 && c->dtype != EVS_DTYPE_BF16) return false;
+    if (c->mode != EVS_MODE_GREEDY && c->mode != EVS_MODE_SAMPLING) return false;
+    if (!(c->temperature > 0.f) || !(c->near_tie_tau >= 0.f)) return false;
+    return true;
+}
+
+evs::Geometry geometry(const evs_config& c) {
+    evs::Geometry g{};
+    g.B = c.batch;
+    g.C = c.n_cand;
+    g.T = c.gamma + 1;
+    g.M_verify = g.B * g.C * g.T;
+    g.M_max = std::max(g.M_verify, g.B * c.prefill_chunk);
+    g.q_max = std::max(g.C * g.T, c.prefill_chunk);
+    g.h_max = 1;
+    for (int i = 0; i < c.n_layers; ++i)
+        if (c.layer_kind[i] == EVS_LAYER_ATTN) g.h_max = std::max(g.h_max, c.layer_param[i]);
+    // prefix split so that splits x sequences x heads covers the 152 SMs about four times
+    const long long target = std::max(1LL, (4LL * 152 + (long long)g.B * g.h_max - 1) / ((long long)g.B * g.h_max));
+    long long chunk = (c.t_max + target - 1) / target;
+    chunk = std::max(64LL, (chunk + 63) / 64 * 64);
+    g.kv_chunk = (int)chunk;
+    g.kv_splits = (int)((c.t_max + chunk - 1) / chunk);
+    return g;
+}
+
+// Lays out every buffer inside the workspace starting at base (or at 0 to size it).
+size_t carve(const evs_config& c, char* base, evs_handle* h) {
+    const evs::Geometry g = geometry(c);
+    const size_t es = elem_bytes(c);
+    const size_t B = c.batch, C = c.n_cand, T = g.T, d = c.d, dh = c.head_dim;
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> char* {
+        char* p = base ? base + off : nullptr;
+        off = align_up(off + bytes);
+        return p;
+    };
+    char* kv_len = take(B * 4);
+    char* kv_base = take(B * 4);
+    char* flags = take(4);
+    char* cand_k = take(B * C * 4);
+    char* cand_corr = take(B * C * 4);
+    char* cand_tie = take(B * C * 4);
+    char* layer_dev = take(sizeof(evs::LayerDesc) * c.n_layers);
+    if (h) {
+        h->kv_len = (int32_t*)kv_len;
+        h->kv_base = (int32_t*)kv_base;
+        h->flags = (uint32_t*)flags;
+        h->cand_k = (int32_t*)cand_k;
+        h->cand_corr = (int32_t*)cand_corr;
+        h->cand_tie = (uint32_t*)cand_tie;
+        h->layer_dev = (evs::LayerDesc*)layer_dev;
+    }
+    for (int i = 0; i < c.n_layers; ++i) {
+        evs::LayerDesc L{};
+        L.kind = c.layer_kind[i];
+        L.param = c.layer_param[i];
+        size_t tail_b = 0, stage_b = 0, state_b = 0, ret_b = 0, cache_b = 0, side_b = 0;
+        if (L.kind == EVS_LAYER_FIR) {
+            tail_b = B * (L.param - 1) * d * 4;
+            stage_b = B * C * (L.param - 1 + T) * d * 4;
+            L.tail = (float*)take(tail_b);
+            L.stage = (float*)take(stage_b);
+        } else if (L.kind == EVS_LAYER_IIR) {
+            state_b = B * d * L.param * 8;
+            ret_b = B * C * T * d * L.param * 8;
+            L.state = (float2*)take(state_b);
+            L.ret = (float2*)take(ret_b);
+        } else {
+            cache_b = B * (size_t)L.param * (size_t)c.t_max * dh * es;
+            L.kc = take(cache_b);
+            L.vc = take(cache_b);
+            if (C > 1) {
+                side_b = B * C * (size_t)L.param * T * dh * es;
+                L.ks = take(side_b);
+                L.vs = take(side_b);
+            }
+        }
+        if (h) {
+            h->layer[i] = L;
+            h->tail_bytes[i] = tail_b;
+            h->stage_bytes[i] = stage_b;
+            h->state_bytes[i] = state_b;
+            h->ret_bytes[i] = ret_b;
+            h->cache_bytes[i] = cache_b;
+            h->side_bytes[i] = side_b;
+        }
+    }
+    char* hbuf = take((size_t)g.M_max * d * 4);
+    char* act = take((size_t)g.M_max * d * es);
+    char* y = take((size_t)g.M_max * 3 * d * 4);
+    char* logits = take((size_t)g.M_verify * c.vocab * 4);
+    char* part = take(B * (size_t)g.h_max * g.kv_splits * g.q_max * (dh + 2) * 4);
+    if (h) {
+        h->h = (float*)hbuf;
+        h->act = act;
+        h->y = (float*)y;
+        h->logits = (float*)logits;
+        h->attn_part = (float*)part;
+        h->g = g;
+    }
+    return off;
+}
+
+evs_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? EVS_OK : EVS_ERR_CUDA; }
+
+evs_status after_launch(evs_handle* h) {
+    (void)h;
+    return cuda_ok(cudaGetLastError());
+}
+
+bool weights_ok(const evs_config& c, const evs_weights* w) {
+    if (!w || !w->embed || !w->head) return false;
+    for (int i = 0; i < c.n_layers; ++i) {
+        const evs_layer_weights& L = w->layer[i];
+        switch (c.layer_kind[i]) {
+            case EVS_LAYER_FIR:
+                if (!L.w_in || !L.w_out || !L.fir_taps) return false;
+                break;
+            case EVS_LAYER_IIR:
+                if (!L.w_in || !L.w_out || !L.iir_lambda || !L.iir_b || !L.iir_c) return false;
+                break;
+            default:
+                if (!L.w_qkv || !L.w_o) return false;
+        }
+    }
+    return true;
+}
+
+evs_status zero_state(evs_handle* h) {
+    const evs_config& c = h->cfg;
+    cudaStream_t s = h->stream;
+    if (cudaMemsetAsync(h->kv_len, 0, c.batch * 4, s) != cudaSuccess) return EVS_ERR_CUDA;
+    if (cudaMemsetAsync(h->kv_base, 0, c.batch * 4, s) != cudaSuccess) return EVS_ERR_CUDA;
+    for (int i = 0; i < c.n_layers; ++i) {
+        const evs::LayerDesc& L = h->layer[i];
+        if (L.kind == EVS_LAYER_FIR && cudaMemsetAsync(L.tail, 0, h->tail_bytes[i], s) != cudaSuccess)
+            return EVS_ERR_CUDA;
+        if (L.kind == EVS_LAYER_IIR && cudaMemsetAsync(L.state, 0, h->state_bytes[i], s) != cudaSuccess)
+            return EVS_ERR_CUDA;
+    }
+    h->kv_hi = 0;
+    h->verified = 0;
+    return EVS_OK;
+}
+
+// One block pass through every layer (Lemma 2: a single forward from the pre-round state).
+void run_layers(evs_handle* h, const int32_t* tokens, int tok_stride, const int32_t* anchor,
+                const evs::Pass& p, bool with_head) {
+    const evs_config& c = h->cfg;
+    const int d = c.d;
+    evs::launch_embed(h, tokens, tok_stride, anchor, p);
+    for (int li = 0; li < c.n_layers; ++li) {
+        const evs_layer_weights& W = h->w.layer[li];
+        evs::launch_rmsnorm(h, p);
+        switch (c.layer_kind[li]) {
+            case EVS_LAYER_FIR:
+                evs::launch_gemm(h, h->act, W.w_in, h->y, p.M, d, d, 3 * d, 0);
+                evs::launch_fir(h, li, p);
+                evs::launch_gemm(h, h->act, W.w_out, h->h, p.M, d, d, d, 1);
+                break;
+            case EVS_LAYER_IIR:
+                evs::launch_gemm(h, h->act, W.w_in, h->y, p.M, d, d, 3 * d, 0);
+                evs::launch_iir(h, li, p);
+                evs::launch_gemm(h, h->act, W.w_out, h->h, p.M, d, d, d, 1);
+                break;
+            default:
+                evs::launch_gemm(h, h->act, W.w_qkv, h->y, p.M, 3 * d, d, 3 * d, 0);
+                evs::launch_kv_write(h, li, p);
+                evs::launch_attention(h, li, p);
+                evs::launch_gemm(h, h->act, W.w_o, h->h, p.M, d, d, d, 1);
+        }
+    }
+    if (with_head) {
+        evs::launch_rmsnorm(h, p);
+        evs::launch_gemm(h, h->act, h->w.head, h->logits, p.M, c.vocab, d, c.vocab, 0);
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t evs_workspace_bytes(const evs_config* cfg) {
+    if (!valid_config(cfg)) return 0;
+    return carve(*cfg, nullptr, nullptr);
+}
+
+evs_status evs_create(const evs_config* cfg, const evs_weights* weights, void* workspace, size_t ws_bytes,
+                      void* stream, evs_handle** out) {
+    if (!out) return EVS_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!valid_config(cfg) || !weights_ok(*cfg, weights) || !workspace) return EVS_ERR_INVALID_ARG;
+    if ((uintptr_t)workspace % kAlign) return EVS_ERR_INVALID_ARG;
+    const size_t need = carve(*cfg, nullptr, nullptr);
+    if (ws_bytes < need) return EVS_ERR_CAPACITY;
+    evs_handle* h = (evs_handle*)calloc(1, sizeof(evs_handle));
+    if (!h) return EVS_ERR_INVALID_ARG;
+    h->cfg = *cfg;
+    h->w = *weights;
+    h->stream = (cudaStream_t)stream;
+    h->ws = (char*)workspace;
+    h->ws_bytes = ws_bytes;
+    carve(*cfg, h->ws, h);
+    evs_status st = cuda_ok(cudaMemcpyAsync(h->layer_dev, h->layer, sizeof(evs::LayerDesc) * cfg->n_layers,
+                                            cudaMemcpyHostToDevice, h->stream));
+    if (st == EVS_OK) st = cuda_ok(cudaMemsetAsync(h->flags, 0, 4, h->stream));
+    if (st == EVS_OK) st = zero_state(h);
+    if (st == EVS_OK) st = cuda_ok(cudaStreamSynchronize(h->stream));  // layer table copied from host
+    if (st != EVS_OK) {
+        free(h);
+        return st;
+    }
+    *out = h;
+    return EVS_OK;
+}
+
+void evs_destroy(evs_handle* h) { free(h); }
+
+evs_status evs_set_stream(evs_handle* h, void* stream) {
+    if (!h) return EVS_ERR_INVALID_ARG;
+    h->stream = (cudaStream_t)stream;
+    return EVS_OK;
+}
+
+evs_status evs_reset(evs_handle* h) {
+    if (!h) return EVS_ERR_INVALID_ARG;
+    h->launches = 0;
+    return zero_state(h);
+}
+
+evs_status evs_prefill(evs_handle* h, const int32_t* tokens, int32_t P) {
+    if (!h || P < 0 || (P > 0 && !tokens)) return EVS_ERR_INVALID_ARG;
+    h->launches = 0;
+    if (h->kv_hi + P > h->cfg.t_max) return EVS_ERR_CAPACITY;
+    const int B = h->cfg.batch, chunk = h->cfg.prefill_chunk;
+    for (int off = 0; off < P; off += chunk) {
+        const int T = std::min(chunk, P - off);
+        evs::Pass p{B, 1, T, B * T, 1, 1};
+        run_layers(h, tokens + off, P, nullptr, p, false);
+        evs::launch_advance(h, T);
+    }
+    h->kv_hi += P;
+    h->verified = 0;
+    return after_launch(h);
+}
+
+evs_status evs_verify_block(evs_handle* h, const int32_t* tokens, const int32_t* anchor, const float* q_probs,
+                            const float* uniforms, int32_t* accepted_len, int32_t* correction,
+                            int32_t* best_cand, uint32_t* near_tie) {
+    if (!h || !tokens || !accepted_len || !correction) return EVS_ERR_INVALID_ARG;
+    const evs_config& c = h->cfg;
+    if (c.mode == EVS_MODE_SAMPLING && (!q_probs || !uniforms)) return EVS_ERR_INVALID_ARG;
+    if (c.n_cand > 1 && !best_cand) return EVS_ERR_INVALID_ARG;
+    h->launches = 0;
+    const int T = c.gamma + 1;
+    if (h->kv_hi + T > c.t_max) return EVS_ERR_CAPACITY;
+    evs::Pass p{c.batch, c.n_cand, T, h->g.M_verify, 0, c.n_cand == 1 ? 1 : 0};
+    run_layers(h, tokens, T, anchor, p, true);
+    evs::launch_accept(h, tokens, q_probs, uniforms, accepted_len, correction, best_cand, near_tie);
+    h->verified = 1;
+    return after_launch(h);
+}
+
+evs_status evs_slice_state(evs_handle* h, const int32_t* accepted_len, const int32_t* best_cand) {
+    if (!h || !accepted_len) return EVS_ERR_INVALID_ARG;
+    if (h->cfg.n_cand > 1 && !best_cand) return EVS_ERR_INVALID_ARG;
+    if (!h->verified) return EVS_ERR_STATE;
+    h->launches = 0;
+    evs::launch_slice(h, accepted_len, best_cand);
+    h->kv_hi += h->cfg.gamma + 1;
+    if (h->kv_hi > h->cfg.t_max) h->kv_hi = h->cfg.t_max;
+    h->verified = 0;
+    return after_launch(h);
+}
+
+evs_status evs_import_state(evs_handle* h, const evs_state_view* v) {
+    if (!h || !v || !v->kv_len) return EVS_ERR_INVALID_ARG;
+    const evs_config& c = h->cfg;
+    h->launches = 0;
+    const size_t es = elem_bytes(c), dh = c.head_dim;
+    long long hi = 0;
+    for (int b = 0; b < c.batch; ++b) {
+        const int n = v->kv_len[b];
+        if (n < 0) return EVS_ERR_INVALID_ARG;
+        if (n > c.t_max || n > v->t_stride) return EVS_ERR_CAPACITY;
+        hi = std::max(hi, (long long)n);
+    }
+    for (int i = 0; i < c.n_layers; ++i) {
+        const evs::LayerDesc& L = h->layer[i];
+        if (L.kind == EVS_LAYER_ATTN) {
+            if (!v->k[i] || !v->v[i]) return EVS_ERR_INVALID_ARG;
+        } else if (L.kind == EVS_LAYER_FIR) {
+            if (!v->fir_tail[i]) return EVS_ERR_INVALID_ARG;
+        } else if (!v->iir_state[i]) {
+            return EVS_ERR_INVALID_ARG;
+        }
+    }
+    cudaStream_t s = h->stream;
+    if (cudaMemcpyAsync(h->kv_len, v->kv_len, c.batch * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return EVS_ERR_CUDA;
+    for (int i = 0; i < c.n_layers; ++i) {
+        const evs::LayerDesc& L = h->layer[i];
+        if (L.kind == EVS_LAYER_ATTN) {
+            const size_t H = L.param;
+            for (int b = 0; b < c.batch; ++b) {
+                const size_t n = v->kv_len[b];
+                if (!n) continue;
+                const size_t dpitch = (size_t)c.t_max * dh * es, spitch = (size_t)v->t_stride * dh * es;
+                char* dk = (char*)L.kc + b * H * dpitch;
+                char* dv = (char*)L.vc + b * H * dpitch;
+                const char* sk = (const char*)v->k[i] + b * H * spitch;
+                const char* sv = (const char*)v->v[i] + b * H * spitch;
+                if (cudaMemcpy2DAsync(dk, dpitch, sk, spitch, n * dh * es, H, cudaMemcpyDefault, s) != cudaSuccess ||
+                    cudaMemcpy2DAsync(dv, dpitch, sv, spitch, n * dh * es, H, cudaMemcpyDefault, s) != cudaSuccess)
+                    return EVS_ERR_CUDA;
+            }
+        } else if (L.kind == EVS_LAYER_FIR) {
+            if (cudaMemcpyAsync(L.tail, v->fir_tail[i], h->tail_bytes[i], cudaMemcpyDefault, s) != cudaSuccess)
+                return EVS_ERR_CUDA;
+        } else {
+            if (cudaMemcpyAsync(L.state, v->iir_state[i], h->state_bytes[i], cudaMemcpyDefault, s) != cudaSuccess)
+                return EVS_ERR_CUDA;
+        }
+    }
+    // the host kv_len array may be reused by the caller as soon as this returns
+    if (cudaStreamSynchronize(s) != cudaSuccess) return EVS_ERR_CUDA;
+    h->kv_hi = hi;
+    h->verified = 0;
+    return EVS_OK;
+}
+
+evs_status evs_export_state(evs_handle* h, const evs_state_view* v) {
+    if (!h || !v || !v->kv_len) return EVS_ERR_INVALID_ARG;
+    const evs_config& c = h->cfg;
+    h->launches = 0;
+    cudaStream_t s = h->stream;
+    const size_t es = elem_bytes(c), dh = c.head_dim;
+    if (cudaMemcpyAsync(v->kv_len, h->kv_len, c.batch * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return EVS_ERR_CUDA;
+    for (int b = 0; b < c.batch; ++b)
+        if (v->kv_len[b] > v->t_stride) return EVS_ERR_CAPACITY;
+    for (int i = 0; i < c.n_layers; ++i) {
+        const evs::LayerDesc& L = h->layer[i];
+        if (L.kind == EVS_LAYER_ATTN) {
+            if (!v->k[i] || !v->v[i]) continue;
+            const size_t H = L.param;
+            for (int b = 0; b < c.batch; ++b) {
+                const size_t n = v->kv_len[b];
+                if (!n) continue;
+                const size_t spitch = (size_t)c.t_max * dh * es, dpitch = (size_t)v->t_stride * dh * es;
+                if (cudaMemcpy2DAsync((char*)v->k[i] + b * H * dpitch, dpitch, (const char*)L.kc + b * H * spitch,
+                                      spitch, n * dh * es, H, cudaMemcpyDefault, s) != cudaSuccess ||
+                    cudaMemcpy2DAsync((char*)v->v[i] + b * H * dpitch, dpitch, (const char*)L.vc + b * H * spitch,
+                                      spitch, n * dh * es, H, cudaMemcpyDefault, s) != cudaSuccess)
+                    return EVS_ERR_CUDA;
+            }
+        } else if (L.kind == EVS_LAYER_FIR) {
+            if (v->fir_tail[i] &&
+                cudaMemcpyAsync(v->fir_tail[i], L.tail, h->tail_bytes[i], cudaMemcpyDefault, s) != cudaSuccess)
+                return EVS_ERR_CUDA;
+        } else if (v->iir_state[i] &&
+                   cudaMemcpyAsync(v->iir_state[i], L.state, h->state_bytes[i], cudaMemcpyDefault, s) != cudaSuccess) {
+            return EVS_ERR_CUDA;
+        }
+    }
+    return cuda_ok(cudaStreamSynchronize(s));
+}
+
+evs_status evs_debug_buffer(evs_handle* h, int32_t which, int32_t layer, evs_buffer_info* out) {
+    if (!h || !out) return EVS_ERR_INVALID_ARG;
+    const evs_config& c = h->cfg;
+    const bool per_layer = !(which == EVS_BUF_LOGITS || which == EVS_BUF_KV_LEN || which == EVS_BUF_CAND_K ||
+                             which == EVS_BUF_CAND_CORR);
+    if (per_layer && (layer < 0 || layer >= c.n_layers)) return EVS_ERR_INVALID_ARG;
+    const evs::LayerDesc* L = per_layer ? &h->layer[layer] : nullptr;
+    void* p = nullptr;
+    size_t n = 0;
+    switch (which) {
+        case EVS_BUF_LOGITS: p = h->logits; n = (size_t)h->g.M_verify * c.vocab * 4; break;
+        case EVS_BUF_KV_LEN: p = h->kv_len; n = c.batch * 4; break;
+        case EVS_BUF_CAND_K: p = h->cand_k; n = (size_t)c.batch * c.n_cand * 4; break;
+        case EVS_BUF_CAND_CORR: p = h->cand_corr; n = (size_t)c.batch * c.n_cand * 4; break;
+        case EVS_BUF_FIR_STAGE: p = L->stage; n = h->stage_bytes[layer]; break;
+        case EVS_BUF_FIR_TAIL: p = L->tail; n = h->tail_bytes[layer]; break;
+        case EVS_BUF_IIR_RET: p = L->ret; n = h->ret_bytes[layer]; break;
+        case EVS_BUF_IIR_STATE: p = L->state; n = h->state_bytes[layer]; break;
+        case EVS_BUF_K_CACHE: p = L->kc; n = h->cache_bytes[layer]; break;
+        case EVS_BUF_V_CACHE: p = L->vc; n = h->cache_bytes[layer]; break;
+        case EVS_BUF_K_SIDE: p = L->ks; n = h->side_bytes[layer]; break;
+        case EVS_BUF_V_SIDE: p = L->vs; n = h->side_bytes[layer]; break;
+        default: return EVS_ERR_INVALID_ARG;
+    }
+    if (!p) return EVS_ERR_INVALID_ARG;
+    out->ptr = p;
+    out->bytes = n;
+    return EVS_OK;
+}
+
+evs_status evs_device_flags(evs_handle* h, uint32_t* flags, int32_t clear) {
+    if (!h || !flags) return EVS_ERR_INVALID_ARG;
+    if (cudaMemcpyAsync(flags, h->flags, 4, cudaMemcpyDeviceToHost, h->stream) != cudaSuccess) return EVS_ERR_CUDA;
+    if (clear && cudaMemsetAsync(h->flags, 0, 4, h->stream) != cudaSuccess) return EVS_ERR_CUDA;
+    return cuda_ok(cudaStreamSynchronize(h->stream));
+}
+
+int32_t evs_last_launch_count(evs_handle* h) { return h ? h->launches : 0; }
+
+const char* evs_status_str(evs_status s) {
+    switch (s) {
+        case EVS_OK: return "ok";
+        case EVS_ERR_INVALID_ARG: return "invalid argument";
+        case EVS_ERR_CAPACITY: return "capacity exceeded (KV rows beyond t_max or workspace too small)";
+        case EVS_ERR_STATE: return "call out of order (slice without a preceding verify)";
+        case EVS_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

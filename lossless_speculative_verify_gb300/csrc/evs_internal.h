@@ -1,0 +1,93 @@
+// Internal layout of a handle and the kernel launchers it drives.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/evs.h"
+
+namespace evs {
+
+// Per-layer device pointers, also mirrored into device memory for the slice kernel.
+struct LayerDesc {
+    int32_t kind, param;           // EVS_LAYER_*, L | N | H
+    float* tail;                   // FIR [B][L-1][d]
+    float* stage;                  // FIR [B][C][L-1+T][d]
+    float2* state;                 // IIR [B][d][N]
+    float2* ret;                   // IIR [B][C][T][d][N]
+    void* kc;                      // attn [B][H][t_max][dh]
+    void* vc;
+    void* ks;                      // attn, C > 1: [B][C][H][T][dh]
+    void* vs;
+};
+
+struct Geometry {
+    int B, C, T;      // verify: T = gamma + 1
+    int M_verify;     // B*C*T
+    int M_max;        // max(M_verify, B*prefill_chunk)
+    int q_max;        // max queries per sequence in a pass (C*T or prefill_chunk)
+    int h_max;        // max attention heads over layers
+    int kv_chunk;     // prefix keys per attention split
+    int kv_splits;    // ceil(t_max / kv_chunk)
+};
+
+// A pass runs B sequences x C candidates x T block positions; row m = (b*C + c)*T + i.
+struct Pass {
+    int B, C, T;        // sequences, candidates, positions per candidate
+    int M;              // B*C*T
+    int commit;         // 1: prefill pass, state updated in place (C == 1)
+    int kv_in_cache;    // 1: block K/V rows go to cache rows kv_base[b] + i (C == 1)
+};
+
+}  // namespace evs
+
+struct evs_handle {
+    evs_config cfg;
+    evs_weights w;
+    cudaStream_t stream;
+    char* ws;
+    size_t ws_bytes;
+    evs::Geometry g;
+    // control words (device)
+    int32_t* kv_len;      // [B]
+    int32_t* kv_base;     // [B] readable length at the start of the current pass
+    uint32_t* flags;      // [1]
+    int32_t* cand_k;      // [B*C]
+    int32_t* cand_corr;   // [B*C]
+    uint32_t* cand_tie;   // [B*C]
+    // activations (device)
+    float* h;             // [M_max][d] residual stream
+    void* act;            // [M_max][d] dtype: normalised input or mixer output
+    float* y;             // [M_max][3d] projection outputs
+    float* logits;        // [M_verify][vocab]
+    float* attn_part;     // [B][H_max][splits][q_max][dh + 2]
+    evs::LayerDesc layer[EVS_MAX_LAYERS];
+    evs::LayerDesc* layer_dev;   // device copy
+    // sizes of per-layer buffers (bytes), for evs_debug_buffer
+    size_t stage_bytes[EVS_MAX_LAYERS], ret_bytes[EVS_MAX_LAYERS], cache_bytes[EVS_MAX_LAYERS],
+        side_bytes[EVS_MAX_LAYERS], tail_bytes[EVS_MAX_LAYERS], state_bytes[EVS_MAX_LAYERS];
+    // host bookkeeping
+    long long kv_hi;      // host upper bound of max_b kv_len
+    int verified;         // a verify was enqueued since the last slice / prefill
+    int launches;         // kernels enqueued by the last public call
+};
+
+namespace evs {
+
+// ---- kernel launchers (kernels.cu) --------------------------------------------------------
+void launch_embed(evs_handle* h, const int32_t* tokens, int tok_stride_bc, const int32_t* anchor,
+                  const Pass& p);
+void launch_rmsnorm(evs_handle* h, const Pass& p);
+void launch_gemm(evs_handle* h, const void* A, const void* W, float* Y, int M, int N, int K,
+                 int ldy, int accumulate);
+void launch_fir(evs_handle* h, int layer, const Pass& p);
+void launch_iir(evs_handle* h, int layer, const Pass& p);
+void launch_kv_write(evs_handle* h, int layer, const Pass& p);
+void launch_attention(evs_handle* h, int layer, const Pass& p);
+void launch_accept(evs_handle* h, const int32_t* tokens, const float* q, const float* u,
+                   int32_t* acc, int32_t* corr, int32_t* cand, uint32_t* tie);
+void launch_slice(evs_handle* h, const int32_t* k, const int32_t* cand);
+void launch_advance(evs_handle* h, int T);
+
+}  // namespace evs

@@ -1,0 +1,800 @@
+// Block-forward, acceptance and slicing kernels (CUDA cores), sm_103a.
+//
+// Steps of one verification round (EvSpark summary, Figure 1(c)-(d)): embed the block
+// [anchor, d_1..d_gamma]; per layer RMS-normalise, project, run the mixer (depthwise FIR
+// over [cached tail || block inputs], modal IIR scan keeping every s_t, or causal
+// attention over the readable prefix plus the in-block keys), project back into the
+// residual; then logits, acceptance, and slicing the state at the accepted index k.
+#include "evs_common.cuh"
+
+namespace evs {
+
+// =========================================================================================
+// embedding gather; records the pass's starting KV length
+// =========================================================================================
+template <typename T>
+__global__ void embed_kernel(const T* __restrict__ E, const int32_t* __restrict__ tokens,
+                             int tok_stride_bc, const int32_t* __restrict__ anchor,
+                             float* __restrict__ h, int d, int C, int Tb, int vocab, int B,
+                             const int32_t* __restrict__ kv_len, int32_t* __restrict__ kv_base,
+                             uint32_t* __restrict__ flags) {
+    const int m = blockIdx.x;
+    const int bc = m / Tb, i = m % Tb, b = bc / C;
+    int tok = (i == 0 && anchor != nullptr) ? anchor[b] : tokens[(size_t)bc * tok_stride_bc + i];
+    if (tok < 0 || tok >= vocab) {
+        if (threadIdx.x == 0) atomicOr(flags, (uint32_t)EVS_FLAG_BAD_TOKEN);
+        tok = tok < 0 ? 0 : vocab - 1;
+    }
+    const T* row = E + (size_t)tok * d;
+    float* out = h + (size_t)m * d;
+    for (int c = threadIdx.x; c < d; c += blockDim.x) out[c] = to_f32(row[c]);
+    if (m == 0)
+        for (int j = threadIdx.x; j < B; j += blockDim.x) kv_base[j] = kv_len[j];
+}
+
+// =========================================================================================
+// RMS norm (no gain): act = h / sqrt(mean(h^2) + eps), stored in the projection dtype
+// =========================================================================================
+template <typename T>
+__global__ void rmsnorm_kernel(const float* __restrict__ h, T* __restrict__ out, int d) {
+    __shared__ float red[32];
+    const int m = blockIdx.x;
+    const float* row = h + (size_t)m * d;
+    float ss = 0.f;
+    for (int c = threadIdx.x; c < d; c += blockDim.x) ss += row[c] * row[c];
+    ss = block_sum(ss, red);
+    const float r = rsqrtf(ss / (float)d + 1e-6f);
+    T* o = out + (size_t)m * d;
+    for (int c = threadIdx.x; c < d; c += blockDim.x) o[c] = from_f32<T>(row[c] * r);
+}
+
+// =========================================================================================
+// CUDA-core projection: Y[m][n] (+)= sum_k A[m][k] * W[n][k]   (W out-major)
+// =========================================================================================
+constexpr int GS_BM = 16, GS_BN = 64, GS_BK = 32;
+
+template <typename T>
+__global__ void __launch_bounds__(256) gemm_simt_kernel(const T* __restrict__ A, const T* __restrict__ W,
+                                                        float* __restrict__ Y, int M, int N, int K,
+                                                        int ldy, int accumulate) {
+    __shared__ float As[GS_BM][GS_BK + 1];
+    __shared__ float Ws[GS_BN][GS_BK + 1];
+    const int tid = threadIdx.x;
+    const int m0 = blockIdx.y * GS_BM, n0 = blockIdx.x * GS_BN;
+    const int r = tid / 16, c0 = (tid % 16) * 4;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k0 = 0; k0 < K; k0 += GS_BK) {
+        for (int e = tid; e < GS_BM * GS_BK; e += 256) {
+            const int rr = e / GS_BK, kk = e % GS_BK;
+            const int m = m0 + rr;
+            As[rr][kk] = (m < M && k0 + kk < K) ? to_f32(A[(size_t)m * K + k0 + kk]) : 0.f;
+        }
+        for (int e = tid; e < GS_BN * GS_BK; e += 256) {
+            const int rr = e / GS_BK, kk = e % GS_BK;
+            const int n = n0 + rr;
+            Ws[rr][kk] = (n < N && k0 + kk < K) ? to_f32(W[(size_t)n * K + k0 + kk]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int kk = 0; kk < GS_BK; ++kk) {
+            const float a = As[r][kk];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[j] = fmaf(a, Ws[c0 + j][kk], acc[j]);
+        }
+        __syncthreads();
+    }
+    const int m = m0 + r;
+    if (m >= M) return;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int n = n0 + c0 + j;
+        if (n >= N) continue;
+        float* dst = Y + (size_t)m * ldy + n;
+        *dst = accumulate ? (*dst + acc[j]) : acc[j];
+    }
+}
+
+// =========================================================================================
+// Depthwise FIR over [cached tail || block inputs]: y_t = sum_{j<L} taps[c][j] v_{t-j}.
+// One thread per (sequence-candidate, channel); loads coalesced along the channel.
+// =========================================================================================
+template <typename T>
+__global__ void fir_kernel(const float* __restrict__ Y, int ldy, T* __restrict__ out, int d,
+                           int C, int Tb, int commit, const float* __restrict__ taps, int L,
+                           float* __restrict__ tail, float* __restrict__ stage) {
+    const int ch = blockIdx.x * blockDim.x + threadIdx.x;
+    const int bc = blockIdx.y, b = bc / C;
+    if (ch >= d) return;
+    float w[16], hist[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        w[j] = (j < L) ? taps[(size_t)ch * L + j] : 0.f;
+        hist[j] = (j < L - 1) ? tail[((size_t)b * (L - 1) + j) * d + ch] : 0.f;
+    }
+    const int srows = L - 1 + Tb;
+    float* st = stage + (size_t)bc * srows * d;
+    if (!commit)
+        for (int j = 0; j < L - 1; ++j) st[(size_t)j * d + ch] = hist[j];
+    for (int i = 0; i < Tb; ++i) {
+        const size_t m = (size_t)bc * Tb + i;
+        const float v = Y[m * ldy + ch];
+        float y = w[0] * v;
+        // hist[L-2] = v_{t-1}, ..., hist[0] = v_{t-L+1}
+#pragma unroll
+        for (int j = 1; j < 16; ++j)
+            if (j < L) y = fmaf(w[j], hist[L - 1 - j], y);
+#pragma unroll
+        for (int j = 0; j < 15; ++j)
+            if (j < L - 2) hist[j] = hist[j + 1];
+        hist[L - 2] = v;
+        out[m * d + ch] = from_f32<T>(y);
+        if (!commit) st[(size_t)(L - 1 + i) * d + ch] = v;
+    }
+    if (commit)
+        for (int j = 0; j < L - 1; ++j) tail[((size_t)b * (L - 1) + j) * d + ch] = hist[j];
+}
+
+// =========================================================================================
+// Modal IIR scan s_t = lam * s_{t-1} + b * u_t, y_t = Re sum_n c_n s_{t,n}.
+// N consecutive lanes hold the N poles of one channel; y by a shuffle reduction.
+// Every s_t goes to the retained-state buffer (verify), or the last one to the state
+// (prefill).
+// =========================================================================================
+template <typename T>
+__global__ void iir_kernel(const float* __restrict__ Y, int ldy, T* __restrict__ out, int d,
+                           int N, int C, int Tb, int commit, const float2* __restrict__ lam,
+                           const float2* __restrict__ bb, const float2* __restrict__ cc,
+                           float2* __restrict__ state, float2* __restrict__ ret) {
+    const int g = blockIdx.x * blockDim.x + threadIdx.x;
+    const int bc = blockIdx.y, b = bc / C;
+    if (g >= d * N) return;  // d*N is a multiple of 32: whole warps leave together
+    const int ch = g / N, n = g % N;
+    const float2 l = lam[g], bq = bb[g], cq = cc[g];
+    float2 s = state[(size_t)b * d * N + g];
+    for (int i = 0; i < Tb; ++i) {
+        const size_t m = (size_t)bc * Tb + i;
+        const float u = Y[m * ldy + ch];
+        const float sx = fmaf(l.x, s.x, fmaf(-l.y, s.y, bq.x * u));
+        const float sy = fmaf(l.x, s.y, fmaf(l.y, s.x, bq.y * u));
+        s = make_float2(sx, sy);
+        float part = fmaf(cq.x, s.x, -cq.y * s.y);
+        for (int o = N >> 1; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (n == 0) out[m * d + ch] = from_f32<T>(part);
+        if (!commit) ret[((size_t)bc * Tb + i) * d * N + g] = s;
+    }
+    if (commit) state[(size_t)b * d * N + g] = s;
+}
+
+// =========================================================================================
+// Block K/V rows from the fused QKV projection output into the cache (one candidate)
+// or the per-candidate side buffer.
+// =========================================================================================
+template <typename T>
+__global__ void kv_write_kernel(const float* __restrict__ Y, int ldy, int d, int H, int dh, int C,
+                                int Tb, int in_cache, int t_max, const int32_t* __restrict__ kv_base,
+                                T* __restrict__ kc, T* __restrict__ vc, T* __restrict__ ks,
+                                T* __restrict__ vs, uint32_t* __restrict__ flags) {
+    const int m = blockIdx.y;
+    const int col = blockIdx.x * blockDim.x + threadIdx.x;
+    if (col >= d) return;
+    const int bc = m / Tb, i = m % Tb, b = bc / C;
+    const int hh = col / dh, e = col % dh;
+    const float kval = Y[(size_t)m * ldy + d + col];
+    const float vval = Y[(size_t)m * ldy + 2 * d + col];
+    if (in_cache) {
+        const int t = kv_base[b] + i;
+        if (t >= t_max) {
+            if (col == 0) atomicOr(flags, (uint32_t)EVS_FLAG_KV_OVERFLOW);
+            return;
+        }
+        const size_t o = (((size_t)b * H + hh) * t_max + t) * dh + e;
+        kc[o] = from_f32<T>(kval);
+        vc[o] = from_f32<T>(vval);
+    } else {
+        const size_t o = (((size_t)bc * H + hh) * Tb + i) * dh + e;
+        ks[o] = from_f32<T>(kval);
+        vs[o] = from_f32<T>(vval);
+    }
+}
+
+// =========================================================================================
+// Split-KV attention over the readable prefix (CUDA cores). One CTA per (split, sequence x
+// head, group of 16 queries). Writes unnormalised partial (o, m, l) per query.
+// =========================================================================================
+constexpr int AQ = 16, AK = 64;
+
+template <typename T>
+__global__ void __launch_bounds__(256) attn_split_kernel(
+    const float* __restrict__ Y, int ldy, const T* __restrict__ kc, const T* __restrict__ vc, int H,
+    int dh, int Q, int q_max, int t_max, int chunk, int splits, const int32_t* __restrict__ kv_base,
+    float* __restrict__ part) {
+    __shared__ float qs[AQ][128];
+    __shared__ float kvs[AK][129];
+    __shared__ float ps[AQ][AK];
+    __shared__ float row_m[AQ], row_l[AQ], row_scale[AQ];
+    const int s = blockIdx.x, bh = blockIdx.y, b = bh / H, hh = bh % H;
+    const int q0 = blockIdx.z * AQ;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n = kv_base[b];
+    const int k_lo = s * chunk, k_hi = min(k_lo + chunk, n);
+    const float scale = rsqrtf((float)dh);
+    for (int e = tid; e < AQ * dh; e += 256) {
+        const int r = e / dh, c = e % dh;
+        const int qi = q0 + r;
+        qs[r][c] = (qi < Q) ? Y[((size_t)b * Q + qi) * ldy + hh * dh + c] * scale : 0.f;
+    }
+    if (tid < AQ) { row_m[tid] = -INFINITY; row_l[tid] = 0.f; }
+    // thread -> 8 outputs of O: row tid / 16, columns (tid % 16) + 16 * u
+    const int orow = tid / 16, ocol = tid % 16;
+    float o[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) o[u] = 0.f;
+    const T* kbase = kc + ((size_t)b * H + hh) * t_max * dh;
+    const T* vbase = vc + ((size_t)b * H + hh) * t_max * dh;
+    __syncthreads();
+    for (int t0 = k_lo; t0 < k_hi; t0 += AK) {
+        const int nk = min(AK, k_hi - t0);
+        for (int e = tid; e < AK * dh; e += 256) {
+            const int r = e / dh, c = e % dh;
+            kvs[r][c] = (r < nk) ? to_f32(kbase[(size_t)(t0 + r) * dh + c]) : 0.f;
+        }
+        __syncthreads();
+        {   // scores: thread -> query tid/16, keys (tid%16) + 16u
+            const int r = tid / 16;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = (tid % 16) + 16 * u;
+                float acc = 0.f;
+                for (int c = 0; c < dh; ++c) acc = fmaf(qs[r][c], kvs[j][c], acc);
+                ps[r][j] = (j < nk) ? acc : -INFINITY;
+            }
+        }
+        __syncthreads();
+        // online softmax: warp w owns query rows 2w, 2w+1
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int r = warp * 2 + rr;
+            const float a = ps[r][lane], c2 = ps[r][lane + 32];
+            const float tmax = warp_max(fmaxf(a, c2));
+            const float m_old = row_m[r];
+            const float m_new = fmaxf(m_old, tmax);
+            const float pa = (a == -INFINITY) ? 0.f : __expf(a - m_new);
+            const float pb = (c2 == -INFINITY) ? 0.f : __expf(c2 - m_new);
+            const float tsum = warp_sum(pa + pb);
+            ps[r][lane] = pa;
+            ps[r][lane + 32] = pb;
+            __syncwarp();
+            if (lane == 0) {
+                const float sc = (m_old == -INFINITY) ? 0.f : __expf(m_old - m_new);
+                row_scale[r] = sc;
+                row_l[r] = row_l[r] * sc + tsum;
+                row_m[r] = m_new;
+            }
+        }
+        __syncthreads();
+        for (int e = tid; e < AK * dh; e += 256) {
+            const int r = e / dh, c = e % dh;
+            kvs[r][c] = (r < nk) ? to_f32(vbase[(size_t)(t0 + r) * dh + c]) : 0.f;
+        }
+        __syncthreads();
+        {
+            const float sc = row_scale[orow];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int c = ocol + 16 * u;
+                if (c < dh) {
+                    float acc = o[u] * sc;
+                    for (int j = 0; j < nk; ++j) acc = fmaf(ps[orow][j], kvs[j][c], acc);
+                    o[u] = acc;
+                }
+            }
+        }
+        __syncthreads();
+    }
+    const int qi = q0 + orow;
+    if (qi < Q) {
+        float* dst = part + ((((size_t)b * H + hh) * splits + s) * q_max + qi) * (dh + 2);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int c = ocol + 16 * u;
+            if (c < dh) dst[c] = o[u];
+        }
+        if (ocol == 0) { dst[dh] = row_m[orow]; dst[dh + 1] = row_l[orow]; }
+    }
+}
+
+// Merge the prefix partials with the in-block causal keys of the query's own candidate,
+// normalise, and store o in the projection dtype. One CTA per (sequence x head, query).
+template <typename T>
+__global__ void attn_combine_kernel(const float* __restrict__ Y, int ldy, const T* __restrict__ kc,
+                                    const T* __restrict__ vc, const T* __restrict__ ks,
+                                    const T* __restrict__ vs, int H, int dh, int C, int Tb, int Q,
+                                    int q_max, int t_max, int splits, int chunk, int in_cache,
+                                    const int32_t* __restrict__ kv_base,
+                                    const float* __restrict__ part, T* __restrict__ out, int d) {
+    __shared__ float red[32];
+    __shared__ float sc_blk[128];
+    const int bh = blockIdx.x, qi = blockIdx.y, b = bh / H, hh = bh % H;
+    const int c = qi / Tb, i = qi % Tb;
+    const int e = threadIdx.x;
+    const bool act = e < dh;
+    const int n = kv_base[b];
+    const int used = min((n + chunk - 1) / chunk, splits);  // splits that saw keys
+    float M = -INFINITY;
+    for (int s = 0; s < used; ++s) {
+        const float* p = part + ((((size_t)b * H + hh) * splits + s) * q_max + qi) * (dh + 2);
+        M = fmaxf(M, p[dh]);
+    }
+    // in-block scores q . k_j / sqrt(dh), j = 0..i
+    const float qv = act ? Y[((size_t)b * Q + qi) * ldy + hh * dh + e] : 0.f;
+    const float scale = rsqrtf((float)dh);
+    for (int j = 0; j <= i; ++j) {
+        float kval = 0.f;
+        if (act) {
+            kval = in_cache ? to_f32(kc[(((size_t)b * H + hh) * t_max + n + j) * dh + e])
+                            : to_f32(ks[((((size_t)(b * C + c)) * H + hh) * Tb + j) * dh + e]);
+        }
+        const float sj = block_sum(qv * kval, red) * scale;
+        if (e == 0) sc_blk[j] = sj;
+        M = fmaxf(M, sj);
+    }
+    __syncthreads();
+    float L = 0.f, O = 0.f;
+    for (int s = 0; s < used; ++s) {
+        const float* p = part + ((((size_t)b * H + hh) * splits + s) * q_max + qi) * (dh + 2);
+        const float ms = p[dh];
+        if (ms == -INFINITY) continue;
+        const float w = __expf(ms - M);
+        L = fmaf(p[dh + 1], w, L);
+        if (act) O = fmaf(p[e], w, O);
+    }
+    for (int j = 0; j <= i; ++j) {
+        const float w = __expf(sc_blk[j] - M);
+        L += w;
+        if (act) {
+            const float vval = in_cache ? to_f32(vc[(((size_t)b * H + hh) * t_max + n + j) * dh + e])
+                                        : to_f32(vs[((((size_t)(b * C + c)) * H + hh) * Tb + j) * dh + e]);
+            O = fmaf(w, vval, O);
+        }
+    }
+    if (act) out[((size_t)b * Q + qi) * d + hh * dh + e] = from_f32<T>(O / L);
+}
+
+// =========================================================================================
+// Softmax + acceptance. One CTA (256 threads) per sequence; candidates in turn.
+// =========================================================================================
+constexpr int ACC_THREADS = 256;
+
+struct ArgMax { float v; int i; };
+
+__device__ __forceinline__ ArgMax better(ArgMax a, ArgMax b) {
+    if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
+    return a;
+}
+
+__device__ ArgMax block_argmax(ArgMax a, float* redv, int* redi) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        ArgMax t{__shfl_xor_sync(0xffffffffu, a.v, o), __shfl_xor_sync(0xffffffffu, a.i, o)};
+        a = better(a, t);
+    }
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
+    __syncthreads();
+    if (l == 0) { redv[w] = a.v; redi[w] = a.i; }
+    __syncthreads();
+    ArgMax r{-INFINITY, 0x7fffffff};
+    if (l < nw) r = ArgMax{redv[l], redi[l]};
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        ArgMax t{__shfl_xor_sync(0xffffffffu, r.v, o), __shfl_xor_sync(0xffffffffu, r.i, o)};
+        r = better(r, t);
+    }
+    return r;
+}
+
+__device__ int block_min_int(int v, int* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
+    __syncthreads();
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    int t = (l < nw) ? red[l] : 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t = min(t, __shfl_xor_sync(0xffffffffu, t, o));
+    return t;
+}
+
+__device__ int block_max_int(int v, int* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
+    __syncthreads();
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    int t = (l < nw) ? red[l] : -1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t = max(t, __shfl_xor_sync(0xffffffffu, t, o));
+    return t;
+}
+
+// Inclusive prefix sum over values held as VPT consecutive ids per thread.
+template <int VPT>
+__device__ void block_scan(float (&v)[VPT], float* red, float& total) {
+    float run = 0.f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) { run += v[j]; v[j] = run; }
+    const int l = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    float x = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (l >= o) x += y;
+    }
+    __syncthreads();
+    if (l == 31) red[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        float z = (l < nw) ? red[l] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, z, o);
+            if (l >= o) z += y;
+        }
+        if (l < nw) red[l] = z;
+    }
+    __syncthreads();
+    const float before = (x - run) + (w > 0 ? red[w - 1] : 0.f);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) v[j] += before;
+    total = red[nw - 1];
+}
+
+// Inverse CDF over r (ids tid*VPT + j): smallest id with cumsum > u * sum; if rounding
+// leaves none, the last id with positive mass.
+template <int VPT>
+__device__ int inverse_cdf(float (&r)[VPT], float u, float tau, bool& tie, float* redf, int* redi) {
+    float cum[VPT];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) cum[j] = r[j];
+    float total;
+    block_scan<VPT>(cum, redf, total);
+    const float thr = u * total;
+    int first = 0x7fffffff, lastpos = -1;
+    bool near = false;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int id = threadIdx.x * VPT + j;
+        if (cum[j] > thr && id < first) first = id;
+        if (r[j] > 0.f) lastpos = id;
+        if (tau > 0.f && fabsf(cum[j] - thr) < tau * total) near = true;
+    }
+    first = block_min_int(first, redi);
+    lastpos = block_max_int(lastpos, redi);
+    const int nearany = block_max_int(near ? 1 : 0, redi);
+    tie = tie || nearany;
+    return (first != 0x7fffffff) ? first : lastpos;
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(ACC_THREADS) accept_kernel(
+    const float* __restrict__ logits, int V, int C, int Tb, int gamma, int mode, float inv_temp,
+    float tau, const int32_t* __restrict__ tokens, const float* __restrict__ qprob,
+    const float* __restrict__ unif, int32_t* __restrict__ cand_k, int32_t* __restrict__ cand_corr,
+    uint32_t* __restrict__ cand_tie, int32_t* __restrict__ out_k, int32_t* __restrict__ out_corr,
+    int32_t* __restrict__ out_cand, uint32_t* __restrict__ out_tie, uint32_t* __restrict__ flags) {
+    __shared__ float redf[32];
+    __shared__ int redi[32];
+    __shared__ float redv[32];
+    __shared__ float pd_sh;
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x;
+    int best_c = 0, best_k = -1, best_corr = 0;
+    uint32_t any_tie = 0;
+    for (int c = 0; c < C; ++c) {
+        const int bc = b * C + c;
+        int k = gamma, corr = 0;
+        bool tie = false;
+        for (int j = 0; j <= gamma; ++j) {
+            const float* row = logits + ((size_t)bc * Tb + j) * V;
+            float l[VPT], pr[VPT];
+            float mx = -INFINITY, sq = 0.f;
+#pragma unroll
+            for (int t = 0; t < VPT; ++t) {
+                l[t] = row[tid * VPT + t];
+                mx = fmaxf(mx, l[t] * inv_temp);
+                sq += l[t] * l[t];
+            }
+            mx = block_max(mx, redf);
+            float se = 0.f;
+#pragma unroll
+            for (int t = 0; t < VPT; ++t) { pr[t] = __expf(l[t] * inv_temp - mx); se += pr[t]; }
+            se = block_sum(se, redf);
+            const float inv_se = 1.f / se;
+#pragma unroll
+            for (int t = 0; t < VPT; ++t) pr[t] *= inv_se;
+            if (mode == EVS_MODE_GREEDY) {
+                ArgMax a{-INFINITY, 0x7fffffff};
+#pragma unroll
+                for (int t = 0; t < VPT; ++t) a = better(a, ArgMax{l[t], tid * VPT + t});
+                a = block_argmax(a, redv, redi);
+                if (tau > 0.f) {
+                    ArgMax s2{-INFINITY, 0x7fffffff};
+#pragma unroll
+                    for (int t = 0; t < VPT; ++t)
+                        if (tid * VPT + t != a.i) s2 = better(s2, ArgMax{l[t], tid * VPT + t});
+                    s2 = block_argmax(s2, redv, redi);
+                    const float rms = sqrtf(block_sum(sq, redf) / (float)V);
+                    if (a.v - s2.v < tau * rms) tie = true;
+                }
+                if (j < gamma && tokens[(size_t)bc * Tb + j + 1] == a.i) continue;
+                k = j;
+                corr = a.i;
+                break;
+            } else {
+                const float u_last = unif[(size_t)bc * Tb + gamma];
+                if (j < gamma) {
+                    int dtok = tokens[(size_t)bc * Tb + j + 1];
+                    dtok = dtok < 0 ? 0 : (dtok >= V ? V - 1 : dtok);
+                    const float* qrow = qprob + ((size_t)bc * gamma + j) * V;
+                    if (dtok / VPT == tid) {
+#pragma unroll
+                        for (int t = 0; t < VPT; ++t)
+                            if (tid * VPT + t == dtok) pd_sh = pr[t];
+                    }
+                    __syncthreads();
+                    const float pd = pd_sh;
+                    __syncthreads();
+                    const float lhs = unif[(size_t)bc * Tb + j] * qrow[dtok];
+                    if (tau > 0.f && fabsf(lhs - pd) < tau * pd) tie = true;
+                    if (lhs < pd) continue;
+                    float r[VPT];
+                    float rs = 0.f;
+#pragma unroll
+                    for (int t = 0; t < VPT; ++t) {
+                        r[t] = fmaxf(pr[t] - qrow[tid * VPT + t], 0.f);
+                        rs += r[t];
+                    }
+                    rs = block_sum(rs, redf);
+                    if (!(rs > 0.f)) {
+                        if (tid == 0) atomicOr(flags, (uint32_t)EVS_FLAG_EMPTY_RESIDUAL);
+#pragma unroll
+                        for (int t = 0; t < VPT; ++t) r[t] = pr[t];
+                    }
+                    k = j;
+                    corr = inverse_cdf<VPT>(r, u_last, tau, tie, redf, redi);
+                    break;
+                }
+                k = gamma;
+                corr = inverse_cdf<VPT>(pr, u_last, tau, tie, redf, redi);
+            }
+        }
+        if (tid == 0) {
+            cand_k[bc] = k;
+            cand_corr[bc] = corr;
+            cand_tie[bc] = tie ? 1u : 0u;
+        }
+        if (k > best_k) { best_k = k; best_c = c; best_corr = corr; }
+        any_tie |= tie ? 1u : 0u;
+    }
+    if (tid == 0) {
+        out_k[b] = best_k;
+        out_corr[b] = best_corr;
+        if (out_cand) out_cand[b] = best_c;
+        if (out_tie) out_tie[b] = any_tie;
+    }
+}
+
+// =========================================================================================
+// State slicing at k (Figure 1(d)): FIR tail <- stage rows k+1 .. k+L-1, IIR state <- s_k,
+// and for several candidates the chosen candidate's k+1 block K/V rows into the cache;
+// then kv_len = kv_base + k + 1. Grid (B, blocks); every block strides over the work.
+// =========================================================================================
+template <typename T>
+__global__ void slice_kernel(const LayerDesc* __restrict__ layers, int n_layers, int d, int dh,
+                             int C, int Tb, int gamma, int t_max,
+                             const int32_t* __restrict__ kin, const int32_t* __restrict__ cin,
+                             const int32_t* __restrict__ kv_base, int32_t* __restrict__ kv_len,
+                             uint32_t* __restrict__ flags) {
+    const int b = blockIdx.x;
+    const int k = kin[b];
+    const int c = cin ? cin[b] : 0;
+    if (k < 0 || k > gamma || c < 0 || c >= C) {
+        if (blockIdx.y == 0 && threadIdx.x == 0) atomicOr(flags, (uint32_t)EVS_FLAG_BAD_K);
+        return;
+    }
+    const int bc = b * C + c;
+    const int n0 = kv_base[b];
+    const int stride = gridDim.y * blockDim.x;
+    const int start = blockIdx.y * blockDim.x + threadIdx.x;
+    bool overflow = n0 + k + 1 > t_max;
+    for (int li = 0; li < n_layers; ++li) {
+        const LayerDesc L = layers[li];
+        if (L.kind == EVS_LAYER_FIR) {
+            const int Lm1 = L.param - 1;
+            const float* st = L.stage + (size_t)bc * (Lm1 + Tb) * d;
+            for (int e = start; e < Lm1 * d; e += stride) {
+                const int j = e / d, ch = e % d;
+                L.tail[((size_t)b * Lm1 + j) * d + ch] = st[(size_t)(k + 1 + j) * d + ch];
+            }
+        } else if (L.kind == EVS_LAYER_IIR) {
+            const int n = d * L.param;
+            const float2* src = L.ret + ((size_t)bc * Tb + k) * n;
+            for (int e = start; e < n; e += stride) L.state[(size_t)b * n + e] = src[e];
+        } else if (C > 1 && !overflow) {
+            const int H = L.param;
+            const int per = (k + 1) * dh;
+            for (int e = start; e < H * per; e += stride) {
+                const int hh = e / per, r = e % per;
+                const int j = r / dh, x = r % dh;
+                const size_t src = ((((size_t)bc) * H + hh) * Tb + j) * dh + x;
+                const size_t dst = (((size_t)b * H + hh) * t_max + n0 + j) * dh + x;
+                ((T*)L.kc)[dst] = ((const T*)L.ks)[src];
+                ((T*)L.vc)[dst] = ((const T*)L.vs)[src];
+            }
+        }
+    }
+    if (blockIdx.y == 0 && threadIdx.x == 0) {
+        if (overflow) atomicOr(flags, (uint32_t)EVS_FLAG_KV_OVERFLOW);
+        kv_len[b] = overflow ? t_max : n0 + k + 1;
+    }
+}
+
+__global__ void advance_kernel(const int32_t* __restrict__ kv_base, int32_t* __restrict__ kv_len,
+                               int B, int T, int t_max, uint32_t* __restrict__ flags) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    int nl = kv_base[b] + T;
+    if (nl > t_max) { atomicOr(flags, (uint32_t)EVS_FLAG_KV_OVERFLOW); nl = t_max; }
+    kv_len[b] = nl;
+}
+
+// =========================================================================================
+// launchers
+// =========================================================================================
+static inline bool is_bf16(const evs_handle* h) { return h->cfg.dtype == EVS_DTYPE_BF16; }
+using bf16 = __nv_bfloat16;
+
+void launch_embed(evs_handle* h, const int32_t* tokens, int tok_stride_bc, const int32_t* anchor,
+                  const Pass& p) {
+    const int d = h->cfg.d;
+    if (is_bf16(h))
+        embed_kernel<bf16><<<p.M, 256, 0, h->stream>>>((const bf16*)h->w.embed, tokens, tok_stride_bc,
+            anchor, h->h, d, p.C, p.T, h->cfg.vocab, p.B, h->kv_len, h->kv_base, h->flags);
+    else
+        embed_kernel<float><<<p.M, 256, 0, h->stream>>>((const float*)h->w.embed, tokens, tok_stride_bc,
+            anchor, h->h, d, p.C, p.T, h->cfg.vocab, p.B, h->kv_len, h->kv_base, h->flags);
+    h->launches++;
+}
+
+void launch_rmsnorm(evs_handle* h, const Pass& p) {
+    const int d = h->cfg.d;
+    if (is_bf16(h)) rmsnorm_kernel<bf16><<<p.M, 256, 0, h->stream>>>(h->h, (bf16*)h->act, d);
+    else rmsnorm_kernel<float><<<p.M, 256, 0, h->stream>>>(h->h, (float*)h->act, d);
+    h->launches++;
+}
+
+void launch_gemm(evs_handle* h, const void* A, const void* W, float* Y, int M, int N, int K, int ldy,
+                 int accumulate) {
+    dim3 grid((N + GS_BN - 1) / GS_BN, (M + GS_BM - 1) / GS_BM);
+    if (is_bf16(h))
+        gemm_simt_kernel<bf16><<<grid, 256, 0, h->stream>>>((const bf16*)A, (const bf16*)W, Y, M, N, K, ldy,
+                                                             accumulate);
+    else
+        gemm_simt_kernel<float><<<grid, 256, 0, h->stream>>>((const float*)A, (const float*)W, Y, M, N, K,
+                                                              ldy, accumulate);
+    h->launches++;
+}
+
+void launch_fir(evs_handle* h, int li, const Pass& p) {
+    const int d = h->cfg.d;
+    const LayerDesc& L = h->layer[li];
+    dim3 grid((d + 127) / 128, p.B * p.C);
+    const float* taps = h->w.layer[li].fir_taps;
+    if (is_bf16(h))
+        fir_kernel<bf16><<<grid, 128, 0, h->stream>>>(h->y, 3 * d, (bf16*)h->act, d, p.C, p.T, p.commit, taps,
+                                                       L.param, L.tail, L.stage);
+    else
+        fir_kernel<float><<<grid, 128, 0, h->stream>>>(h->y, 3 * d, (float*)h->act, d, p.C, p.T, p.commit,
+                                                        taps, L.param, L.tail, L.stage);
+    h->launches++;
+}
+
+void launch_iir(evs_handle* h, int li, const Pass& p) {
+    const int d = h->cfg.d;
+    const LayerDesc& L = h->layer[li];
+    const int N = L.param;
+    dim3 grid((d * N + 255) / 256, p.B * p.C);
+    const float2* lam = (const float2*)h->w.layer[li].iir_lambda;
+    const float2* bb = (const float2*)h->w.layer[li].iir_b;
+    const float2* cc = (const float2*)h->w.layer[li].iir_c;
+    if (is_bf16(h))
+        iir_kernel<bf16><<<grid, 256, 0, h->stream>>>(h->y, 3 * d, (bf16*)h->act, d, N, p.C, p.T, p.commit,
+                                                       lam, bb, cc, L.state, L.ret);
+    else
+        iir_kernel<float><<<grid, 256, 0, h->stream>>>(h->y, 3 * d, (float*)h->act, d, N, p.C, p.T, p.commit,
+                                                        lam, bb, cc, L.state, L.ret);
+    h->launches++;
+}
+
+void launch_kv_write(evs_handle* h, int li, const Pass& p) {
+    const int d = h->cfg.d;
+    const LayerDesc& L = h->layer[li];
+    const int H = L.param, dh = h->cfg.head_dim;
+    dim3 grid((d + 255) / 256, p.M);
+    if (is_bf16(h))
+        kv_write_kernel<bf16><<<grid, 256, 0, h->stream>>>(h->y, 3 * d, d, H, dh, p.C, p.T, p.kv_in_cache,
+            h->cfg.t_max, h->kv_base, (bf16*)L.kc, (bf16*)L.vc, (bf16*)L.ks, (bf16*)L.vs, h->flags);
+    else
+        kv_write_kernel<float><<<grid, 256, 0, h->stream>>>(h->y, 3 * d, d, H, dh, p.C, p.T, p.kv_in_cache,
+            h->cfg.t_max, h->kv_base, (float*)L.kc, (float*)L.vc, (float*)L.ks, (float*)L.vs, h->flags);
+    h->launches++;
+}
+
+void launch_attention(evs_handle* h, int li, const Pass& p) {
+    const int d = h->cfg.d;
+    const LayerDesc& L = h->layer[li];
+    const int H = L.param, dh = h->cfg.head_dim;
+    const int Q = p.C * p.T;
+    const Geometry& g = h->g;
+    dim3 grid(g.kv_splits, p.B * H, (Q + AQ - 1) / AQ);
+    if (is_bf16(h))
+        attn_split_kernel<bf16><<<grid, 256, 0, h->stream>>>(h->y, 3 * d, (const bf16*)L.kc, (const bf16*)L.vc,
+            H, dh, Q, g.q_max, h->cfg.t_max, g.kv_chunk, g.kv_splits, h->kv_base, h->attn_part);
+    else
+        attn_split_kernel<float><<<grid, 256, 0, h->stream>>>(h->y, 3 * d, (const float*)L.kc,
+            (const float*)L.vc, H, dh, Q, g.q_max, h->cfg.t_max, g.kv_chunk, g.kv_splits, h->kv_base,
+            h->attn_part);
+    h->launches++;
+    dim3 grid2(p.B * H, Q);
+    const int thr = dh < 32 ? 32 : dh;
+    if (is_bf16(h))
+        attn_combine_kernel<bf16><<<grid2, thr, 0, h->stream>>>(h->y, 3 * d, (const bf16*)L.kc,
+            (const bf16*)L.vc, (const bf16*)L.ks, (const bf16*)L.vs, H, dh, p.C, p.T, Q, g.q_max, h->cfg.t_max,
+            g.kv_splits, g.kv_chunk, p.kv_in_cache, h->kv_base, h->attn_part, (bf16*)h->act, d);
+    else
+        attn_combine_kernel<float><<<grid2, thr, 0, h->stream>>>(h->y, 3 * d, (const float*)L.kc,
+            (const float*)L.vc, (const float*)L.ks, (const float*)L.vs, H, dh, p.C, p.T, Q, g.q_max,
+            h->cfg.t_max, g.kv_splits, g.kv_chunk, p.kv_in_cache, h->kv_base, h->attn_part, (float*)h->act, d);
+    h->launches++;
+}
+
+void launch_accept(evs_handle* h, const int32_t* tokens, const float* q, const float* u, int32_t* acc,
+                   int32_t* corr, int32_t* cand, uint32_t* tie) {
+    const evs_config& c = h->cfg;
+    const int V = c.vocab;
+    const float inv_t = 1.0f / c.temperature;
+    const int Tb = c.gamma + 1;
+#define EVS_ACC(VPT)                                                                              \
+    accept_kernel<VPT><<<c.batch, ACC_THREADS, 0, h->stream>>>(h->logits, V, c.n_cand, Tb, c.gamma,   \
+        c.mode, inv_t, c.near_tie_tau, tokens, q, u, h->cand_k, h->cand_corr, h->cand_tie, acc, corr, \
+        cand, tie, h->flags)
+    switch (V / ACC_THREADS) {
+        case 1: EVS_ACC(1); break;
+        case 2: EVS_ACC(2); break;
+        case 4: EVS_ACC(4); break;
+        case 8: EVS_ACC(8); break;
+        default: EVS_ACC(16); break;
+    }
+#undef EVS_ACC
+    h->launches++;
+}
+
+void launch_slice(evs_handle* h, const int32_t* k, const int32_t* cand) {
+    const evs_config& c = h->cfg;
+    dim3 grid(c.batch, 16);
+    if (is_bf16(h))
+        slice_kernel<bf16><<<grid, 256, 0, h->stream>>>(h->layer_dev, c.n_layers, c.d, c.head_dim, c.n_cand,
+            c.gamma + 1, c.gamma, c.t_max, k, cand, h->kv_base, h->kv_len, h->flags);
+    else
+        slice_kernel<float><<<grid, 256, 0, h->stream>>>(h->layer_dev, c.n_layers, c.d, c.head_dim, c.n_cand,
+            c.gamma + 1, c.gamma, c.t_max, k, cand, h->kv_base, h->kv_len, h->flags);
+    h->launches++;
+}
+
+void launch_advance(evs_handle* h, int T) {
+    advance_kernel<<<1, 256, 0, h->stream>>>(h->kv_base, h->kv_len, h->cfg.batch, T, h->cfg.t_max, h->flags);
+    h->launches++;
+}
+
+}  // namespace evs
