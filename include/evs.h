@@ -220,6 +220,21 @@ evs_status evs_debug_buffer(evs_handle* h, int32_t which, int32_t layer, evs_buf
  * clear != 0. */
 evs_status evs_device_flags(evs_handle* h, uint32_t* flags, int32_t clear);
 
+/* Kernel kinds for per-kind timing. */
+enum {
+    EVS_K_EMBED = 0, EVS_K_NORM = 1, EVS_K_GEMM = 2, EVS_K_FIR = 3, EVS_K_IIR = 4,
+    EVS_K_KV_WRITE = 5, EVS_K_ATTN = 6, EVS_K_ATTN_COMBINE = 7, EVS_K_ACCEPT = 8,
+    EVS_K_SLICE = 9, EVS_K_ADVANCE = 10, EVS_K_COUNT = 11
+};
+
+/* Per-kernel-kind timing with CUDA events (tracing for measurement; the pages describe no
+ * tracing mechanism). While enabled, every launch is bracketed by two events recorded on
+ * the handle's stream, so calls must not be captured into a CUDA graph. evs_profile_read
+ * synchronises the stream and returns, for each kind < n, the launches and summed
+ * milliseconds since the previous read, then clears the counters. */
+evs_status evs_profile_enable(evs_handle* h, int32_t on);
+evs_status evs_profile_read(evs_handle* h, int32_t* launches, float* ms, int32_t n);
+
 /* Number of kernel launches the last public call enqueued (for accounting). */
 int32_t evs_last_launch_count(evs_handle* h);
 

@@ -5,8 +5,53 @@
 #include <string.h>
 
 #include <algorithm>
+#include <vector>
 
 #include "evs_internal.h"
+
+namespace evs {
+
+// Event pairs around launches, grouped by kernel kind (evs_profile_*).
+struct Profiler {
+    struct Rec { int kind; cudaEvent_t a, b; };
+    std::vector<Rec> recs;
+    std::vector<cudaEvent_t> pool;
+    cudaEvent_t open = nullptr;
+    cudaEvent_t get() {
+        if (!pool.empty()) {
+            cudaEvent_t e = pool.back();
+            pool.pop_back();
+            return e;
+        }
+        cudaEvent_t e = nullptr;
+        cudaEventCreate(&e);
+        return e;
+    }
+    ~Profiler() {
+        for (auto& r : recs) { cudaEventDestroy(r.a); cudaEventDestroy(r.b); }
+        for (auto e : pool) cudaEventDestroy(e);
+        if (open) cudaEventDestroy(open);
+    }
+};
+
+void prof_begin(evs_handle* h, int kind) {
+    (void)kind;
+    if (!h->prof_on) return;
+    Profiler* p = (Profiler*)h->prof;
+    p->open = p->get();
+    cudaEventRecord(p->open, h->stream);
+}
+
+void prof_end(evs_handle* h, int kind) {
+    if (!h->prof_on) return;
+    Profiler* p = (Profiler*)h->prof;
+    cudaEvent_t e = p->get();
+    cudaEventRecord(e, h->stream);
+    p->recs.push_back({kind, p->open, e});
+    p->open = nullptr;
+}
+
+}  // namespace evs
 
 namespace {
 
@@ -257,7 +302,35 @@ evs_status evs_create(const evs_config* cfg, const evs_weights* weights, void* w
     return EVS_OK;
 }
 
-void evs_destroy(evs_handle* h) { free(h); }
+void evs_destroy(evs_handle* h) {
+    if (!h) return;
+    delete (evs::Profiler*)h->prof;
+    free(h);
+}
+
+evs_status evs_profile_enable(evs_handle* h, int32_t on) {
+    if (!h) return EVS_ERR_INVALID_ARG;
+    if (on && !h->prof) h->prof = new evs::Profiler();
+    h->prof_on = on ? 1 : 0;
+    return EVS_OK;
+}
+
+evs_status evs_profile_read(evs_handle* h, int32_t* launches, float* ms, int32_t n) {
+    if (!h || !launches || !ms || n < 0) return EVS_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) { launches[i] = 0; ms[i] = 0.f; }
+    evs::Profiler* p = (evs::Profiler*)h->prof;
+    if (!p) return EVS_OK;
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess) return EVS_ERR_CUDA;
+    for (auto& r : p->recs) {
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) return EVS_ERR_CUDA;
+        if (r.kind >= 0 && r.kind < n) { launches[r.kind] += 1; ms[r.kind] += t; }
+        p->pool.push_back(r.a);
+        p->pool.push_back(r.b);
+    }
+    p->recs.clear();
+    return EVS_OK;
+}
 
 evs_status evs_set_stream(evs_handle* h, void* stream) {
     if (!h) return EVS_ERR_INVALID_ARG;

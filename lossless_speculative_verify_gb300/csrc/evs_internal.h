@@ -71,9 +71,15 @@ struct evs_handle {
     long long kv_hi;      // host upper bound of max_b kv_len
     int verified;         // a verify was enqueued since the last slice / prefill
     int launches;         // kernels enqueued by the last public call
+    void* prof;           // evs::Profiler*, lazily created
+    int prof_on;
 };
 
 namespace evs {
+
+// ---- per-kind event timing (evs_api.cu) --------------------------------------------------
+void prof_begin(evs_handle* h, int kind);
+void prof_end(evs_handle* h, int kind);
 
 // ---- kernel launchers (kernels.cu) --------------------------------------------------------
 void launch_embed(evs_handle* h, const int32_t* tokens, int tok_stride_bc, const int32_t* anchor,

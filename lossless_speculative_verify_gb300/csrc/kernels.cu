@@ -657,6 +657,7 @@ using bf16 = __nv_bfloat16;
 
 void launch_embed(evs_handle* h, const int32_t* tokens, int tok_stride_bc, const int32_t* anchor,
                   const Pass& p) {
+    prof_begin(h, EVS_K_EMBED);
     const int d = h->cfg.d;
     if (is_bf16(h))
         embed_kernel<bf16><<<p.M, 256, 0, h->stream>>>((const bf16*)h->w.embed, tokens, tok_stride_bc,
@@ -665,17 +666,21 @@ void launch_embed(evs_handle* h, const int32_t* tokens, int tok_stride_bc, const
         embed_kernel<float><<<p.M, 256, 0, h->stream>>>((const float*)h->w.embed, tokens, tok_stride_bc,
             anchor, h->h, d, p.C, p.T, h->cfg.vocab, p.B, h->kv_len, h->kv_base, h->flags);
     h->launches++;
+    prof_end(h, EVS_K_EMBED);
 }
 
 void launch_rmsnorm(evs_handle* h, const Pass& p) {
+    prof_begin(h, EVS_K_NORM);
     const int d = h->cfg.d;
     if (is_bf16(h)) rmsnorm_kernel<bf16><<<p.M, 256, 0, h->stream>>>(h->h, (bf16*)h->act, d);
     else rmsnorm_kernel<float><<<p.M, 256, 0, h->stream>>>(h->h, (float*)h->act, d);
     h->launches++;
+    prof_end(h, EVS_K_NORM);
 }
 
 void launch_gemm(evs_handle* h, const void* A, const void* W, float* Y, int M, int N, int K, int ldy,
                  int accumulate) {
+    prof_begin(h, EVS_K_GEMM);
     dim3 grid((N + GS_BN - 1) / GS_BN, (M + GS_BM - 1) / GS_BM);
     if (is_bf16(h))
         gemm_simt_kernel<bf16><<<grid, 256, 0, h->stream>>>((const bf16*)A, (const bf16*)W, Y, M, N, K, ldy,
@@ -684,9 +689,11 @@ void launch_gemm(evs_handle* h, const void* A, const void* W, float* Y, int M, i
         gemm_simt_kernel<float><<<grid, 256, 0, h->stream>>>((const float*)A, (const float*)W, Y, M, N, K,
                                                               ldy, accumulate);
     h->launches++;
+    prof_end(h, EVS_K_GEMM);
 }
 
 void launch_fir(evs_handle* h, int li, const Pass& p) {
+    prof_begin(h, EVS_K_FIR);
     const int d = h->cfg.d;
     const LayerDesc& L = h->layer[li];
     dim3 grid((d + 127) / 128, p.B * p.C);
@@ -698,9 +705,11 @@ void launch_fir(evs_handle* h, int li, const Pass& p) {
         fir_kernel<float><<<grid, 128, 0, h->stream>>>(h->y, 3 * d, (float*)h->act, d, p.C, p.T, p.commit,
                                                         taps, L.param, L.tail, L.stage);
     h->launches++;
+    prof_end(h, EVS_K_FIR);
 }
 
 void launch_iir(evs_handle* h, int li, const Pass& p) {
+    prof_begin(h, EVS_K_IIR);
     const int d = h->cfg.d;
     const LayerDesc& L = h->layer[li];
     const int N = L.param;
@@ -715,9 +724,11 @@ void launch_iir(evs_handle* h, int li, const Pass& p) {
         iir_kernel<float><<<grid, 256, 0, h->stream>>>(h->y, 3 * d, (float*)h->act, d, N, p.C, p.T, p.commit,
                                                         lam, bb, cc, L.state, L.ret);
     h->launches++;
+    prof_end(h, EVS_K_IIR);
 }
 
 void launch_kv_write(evs_handle* h, int li, const Pass& p) {
+    prof_begin(h, EVS_K_KV_WRITE);
     const int d = h->cfg.d;
     const LayerDesc& L = h->layer[li];
     const int H = L.param, dh = h->cfg.head_dim;
@@ -729,9 +740,11 @@ void launch_kv_write(evs_handle* h, int li, const Pass& p) {
         kv_write_kernel<float><<<grid, 256, 0, h->stream>>>(h->y, 3 * d, d, H, dh, p.C, p.T, p.kv_in_cache,
             h->cfg.t_max, h->kv_base, (float*)L.kc, (float*)L.vc, (float*)L.ks, (float*)L.vs, h->flags);
     h->launches++;
+    prof_end(h, EVS_K_KV_WRITE);
 }
 
 void launch_attention(evs_handle* h, int li, const Pass& p) {
+    prof_begin(h, EVS_K_ATTN);
     const int d = h->cfg.d;
     const LayerDesc& L = h->layer[li];
     const int H = L.param, dh = h->cfg.head_dim;
@@ -746,6 +759,8 @@ void launch_attention(evs_handle* h, int li, const Pass& p) {
             (const float*)L.vc, H, dh, Q, g.q_max, h->cfg.t_max, g.kv_chunk, g.kv_splits, h->kv_base,
             h->attn_part);
     h->launches++;
+    prof_end(h, EVS_K_ATTN);
+    prof_begin(h, EVS_K_ATTN_COMBINE);
     dim3 grid2(p.B * H, Q);
     const int thr = dh < 32 ? 32 : dh;
     if (is_bf16(h))
@@ -757,10 +772,12 @@ void launch_attention(evs_handle* h, int li, const Pass& p) {
             (const float*)L.vc, (const float*)L.ks, (const float*)L.vs, H, dh, p.C, p.T, Q, g.q_max,
             h->cfg.t_max, g.kv_splits, g.kv_chunk, p.kv_in_cache, h->kv_base, h->attn_part, (float*)h->act, d);
     h->launches++;
+    prof_end(h, EVS_K_ATTN_COMBINE);
 }
 
 void launch_accept(evs_handle* h, const int32_t* tokens, const float* q, const float* u, int32_t* acc,
                    int32_t* corr, int32_t* cand, uint32_t* tie) {
+    prof_begin(h, EVS_K_ACCEPT);
     const evs_config& c = h->cfg;
     const int V = c.vocab;
     const float inv_t = 1.0f / c.temperature;
@@ -778,9 +795,11 @@ void launch_accept(evs_handle* h, const int32_t* tokens, const float* q, const f
     }
 #undef EVS_ACC
     h->launches++;
+    prof_end(h, EVS_K_ACCEPT);
 }
 
 void launch_slice(evs_handle* h, const int32_t* k, const int32_t* cand) {
+    prof_begin(h, EVS_K_SLICE);
     const evs_config& c = h->cfg;
     dim3 grid(c.batch, 16);
     if (is_bf16(h))
@@ -790,11 +809,14 @@ void launch_slice(evs_handle* h, const int32_t* k, const int32_t* cand) {
         slice_kernel<float><<<grid, 256, 0, h->stream>>>(h->layer_dev, c.n_layers, c.d, c.head_dim, c.n_cand,
             c.gamma + 1, c.gamma, c.t_max, k, cand, h->kv_base, h->kv_len, h->flags);
     h->launches++;
+    prof_end(h, EVS_K_SLICE);
 }
 
 void launch_advance(evs_handle* h, int T) {
+    prof_begin(h, EVS_K_ADVANCE);
     advance_kernel<<<1, 256, 0, h->stream>>>(h->kv_base, h->kv_len, h->cfg.batch, T, h->cfg.t_max, h->flags);
     h->launches++;
+    prof_end(h, EVS_K_ADVANCE);
 }
 
 }  // namespace evs

@@ -1,0 +1,165 @@
+"""Shared helpers for the GPU parity tests: build an oracle / library pair on the same
+seeded inputs and compare them."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from synth import gen_prefix, gen_round, gen_state, gen_weights
+
+# Tolerances (relative L2 error per tensor): fp32 1e-5, bf16 2e-2.
+TOL = {"f32": 1e-5, "bf16": 2e-2}
+# Near-tie thresholds used when comparing discrete decisions.
+TAU = {"f32": 1e-5, "bf16": 2e-2}
+
+
+def rel_l2(a, b) -> float:
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    nb = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / (nb if nb > 0 else 1.0))
+
+
+def layer_list(wl):
+    return [(s.kind, s.param) for s in wl.layers]
+
+
+def make_verifier(wl, weights, t_max, near_tie_tau=None):
+    from lossless_speculative_verify_gb300 import DeviceWeights, Verifier, make_config
+    tau = TAU[wl.dtype] if near_tie_tau is None else near_tie_tau
+    cfg = make_config(wl.d, layer_list(wl), wl.head_dim, wl.gamma, wl.batch, wl.n_cand, t_max,
+                      wl.prefill_chunk, wl.dtype, wl.mode, wl.temperature, tau, wl.vocab)
+    dw = DeviceWeights(layer_list(wl), weights, wl.dtype)
+    return Verifier(cfg, dw)
+
+
+class Pair:
+    """Oracle and library driven in lockstep."""
+
+    def __init__(self, wl, t_max=None, weights=None):
+        self.wl = wl
+        self.weights = gen_weights(wl) if weights is None else weights
+        self.tgt = oracle.Target(wl, self.weights)
+        self.t_max = t_max or (wl.prefix_len + 16 * (wl.gamma + 1))
+        self.ver = make_verifier(wl, self.weights, self.t_max)
+        self.states = [self.tgt.empty_state() for _ in range(wl.batch)]
+
+    # ---- state ---------------------------------------------------------------------------
+    def prefill(self, P):
+        toks = gen_prefix(self.wl, P)
+        for b in range(self.wl.batch):
+            oracle.prefill(self.tgt, self.states[b], toks[b])
+        self.ver.prefill(torch.as_tensor(toks, dtype=torch.int32).cuda().contiguous())
+
+    def import_synthetic(self, P):
+        st = gen_state(self.wl, P)
+        self.states = [self.tgt.state_from_arrays(st, b) for b in range(self.wl.batch)]
+        self.ver.import_state(st)
+
+    def oracle_state_arrays(self):
+        """Oracle states in the library's import/export format."""
+        B = self.wl.batch
+        n = max(s.kv_len or 0 for s in self.states)
+        out = {"kv_len": np.array([s.kv_len or 0 for s in self.states], np.int32), "layers": []}
+        for li, spec in enumerate(self.wl.layers):
+            if spec.kind == "attn":
+                H, dh = spec.param, self.wl.head_dim
+                K = np.zeros((B, H, n, dh))
+                V = np.zeros((B, H, n, dh))
+                for b, s in enumerate(self.states):
+                    kv = s.layers[li]["kv"]
+                    K[b, :, :kv.length] = kv.k[:, :kv.length]
+                    V[b, :, :kv.length] = kv.v[:, :kv.length]
+                out["layers"].append({"kind": "attn", "k": K, "v": V})
+            elif spec.kind == "fir":
+                out["layers"].append({"kind": "fir",
+                                      "tail": np.stack([s.layers[li]["tail"] for s in self.states])})
+            else:
+                out["layers"].append({"kind": "iir",
+                                      "s": np.stack([s.layers[li]["s"] for s in self.states])})
+        return out
+
+    def compare_state(self, tol=None):
+        tol = TOL[self.wl.dtype] if tol is None else tol
+        g = self.ver.export_state()
+        o = self.oracle_state_arrays()
+        np.testing.assert_array_equal(g["kv_len"], o["kv_len"])
+        worst = 0.0
+        for li, (a, b) in enumerate(zip(g["layers"], o["layers"])):
+            if a["kind"] == "attn":
+                for bb in range(self.wl.batch):
+                    n = int(o["kv_len"][bb])
+                    for key in ("k", "v"):
+                        e = rel_l2(a[key][bb, :, :n], b[key][bb, :, :n])
+                        assert e <= tol, f"layer {li} {key} seq {bb}: rel err {e:.3e}"
+                        worst = max(worst, e)
+            elif a["kind"] == "fir":
+                e = rel_l2(a["tail"], b["tail"])
+                assert e <= tol, f"layer {li} FIR tail: rel err {e:.3e}"
+                worst = max(worst, e)
+            else:
+                e = rel_l2(np.stack([a["s"].real, a["s"].imag]), np.stack([b["s"].real, b["s"].imag]))
+                assert e <= tol, f"layer {li} IIR state: rel err {e:.3e}"
+                worst = max(worst, e)
+        return worst
+
+    # ---- one round -------------------------------------------------------------------------
+    def round_inputs(self, r, anchor=None):
+        rnd = gen_round(self.wl, r, anchor=anchor)
+        return rnd
+
+    def run_round(self, rnd, check_block=True, tol=None):
+        """Verify + slice on both sides from the current (identical) state. Returns
+        (oracle result, gpu k, gpu corr, gpu cand, near_tie_oracle)."""
+        wl = self.wl
+        tol = TOL[wl.dtype] if tol is None else tol
+        tau = TAU[wl.dtype]
+        dev = lambda a, dt: torch.as_tensor(a, dtype=dt).cuda().contiguous()
+        toks = dev(rnd["tokens"], torch.int32)
+        q = dev(rnd["q"], torch.float32) if wl.mode == "sampling" else None
+        u = dev(rnd["u"], torch.float32) if wl.mode == "sampling" else None
+        pre = [s.snapshot() for s in self.states]
+        res = oracle.verify_round(self.tgt, self.states, rnd["tokens"], rnd["q"], rnd["u"], wl.mode,
+                                  wl.temperature, tau)
+        k, corr, cand, tie = self.ver.verify(toks, q, u)
+        torch.cuda.synchronize()
+        if check_block:
+            self.check_block(res, tol)
+        gk, gc, gcand = k.cpu().numpy(), corr.cpu().numpy(), cand.cpu().numpy()
+        self.ver.slice(k, cand)
+        return res, gk, gc, gcand
+
+    def check_block(self, res, tol):
+        """Block forward outputs: logits, retained IIR states, FIR inputs, block K/V."""
+        wl = self.wl
+        B, C, T, V, d = wl.batch, wl.n_cand, wl.block, wl.vocab, wl.d
+        lg = self.ver.buffer(0, -1, torch.float32, (B, C, T, V)).cpu().numpy()
+        e = rel_l2(lg, res.logits)
+        assert e <= tol, f"logits rel err {e:.3e}"
+        for li, spec in enumerate(wl.layers):
+            if spec.kind == "iir":
+                N = spec.param
+                ret = self.ver.buffer(2, li, torch.float32, (B, C, T, d, N, 2)).cpu().numpy()
+                ref = np.array([[[res.traces[b][c][i][li]["s"] for i in range(T)] for c in range(C)]
+                                for b in range(B)])
+                e = rel_l2(ret, np.stack([ref.real, ref.imag], axis=-1))
+                assert e <= tol, f"layer {li} retained IIR states rel err {e:.3e}"
+            elif spec.kind == "fir":
+                Lm1 = spec.param - 1
+                stage = self.ver.buffer(1, li, torch.float32, (B, C, Lm1 + T, d)).cpu().numpy()
+                ref = np.array([[[res.traces[b][c][i][li]["v"] for i in range(T)] for c in range(C)]
+                                for b in range(B)])
+                e = rel_l2(stage[:, :, Lm1:], ref)
+                assert e <= tol, f"layer {li} FIR block inputs rel err {e:.3e}"
+            elif C > 1:
+                H, dh = spec.param, wl.head_dim
+                tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+                ks = self.ver.buffer(5, li, tdt, (B, C, H, T, dh)).float().cpu().numpy()
+                ref = np.array([[[res.traces[b][c][i][li]["k"] for i in range(T)] for c in range(C)]
+                                for b in range(B)])                       # [B,C,T,H,dh]
+                e = rel_l2(ks, ref.transpose(0, 1, 3, 2, 4))
+                assert e <= tol, f"layer {li} block keys rel err {e:.3e}"
+
+    def resync_from_oracle(self):
+        self.ver.import_state(self.oracle_state_arrays())

@@ -1,0 +1,184 @@
+"""GPU parity: the CUDA path through the C-ABI against the fp64 oracle, element by
+element on the same seeded inputs. Tolerances: relative L2 error per tensor <= 1e-5 (fp32)
+or 2e-2 (bf16) on logits, retained IIR states, FIR inputs, K/V and sliced states; accepted
+lengths, corrections, candidates, KV lengths and slice indices exact, except on rounds the
+oracle flags as near-ties (counted, and the library is then re-synchronised)."""
+import numpy as np
+import pytest
+import torch
+
+from synth import LayerSpec, gen_round, get_workload
+from gpu_harness import Pair, TOL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from lossless_speculative_verify_gb300.build import build
+    build()
+
+
+def _lockstep(pair, rounds, first_round=0, drafts=None):
+    """Run rounds on both sides; anchor = previous correction. Returns near-tie count."""
+    ties = 0
+    anchor = None
+    for r in range(first_round, first_round + rounds):
+        rnd = gen_round(pair.wl, r, anchor=anchor)
+        if drafts is not None:
+            rnd["tokens"] = drafts(pair, rnd)
+        res, gk, gc, gcand = pair.run_round(rnd)
+        if res.tie.any():
+            ties += 1
+            pair.resync_from_oracle()
+        else:
+            np.testing.assert_array_equal(gk, res.k)
+            np.testing.assert_array_equal(gc, res.corr)
+            if pair.wl.n_cand > 1:
+                np.testing.assert_array_equal(gcand, res.cand)
+            pair.compare_state()
+        anchor = res.corr
+    return ties
+
+
+def identity_drafts(pair, rnd, wrong_at=None):
+    """Drafts equal to the oracle's greedy chain (optionally wrong at one position)."""
+    toks = rnd["tokens"].copy()
+    B, C, T = toks.shape
+    for b in range(B):
+        for c in range(C):
+            probe = pair.states[b].clone()
+            for i in range(T - 1):
+                nxt = int(np.argmax(pair.tgt.step(probe, int(toks[b, c, i]))))
+                w = wrong_at if np.isscalar(wrong_at) or wrong_at is None else wrong_at[c]
+                if w is not None and i == w:
+                    nxt = (nxt + 1) % pair.wl.vocab
+                toks[b, c, i + 1] = nxt
+    return toks
+
+
+def test_tiny_fp32_prefill_matches_oracle():
+    wl = get_workload("tiny_d64_fp32")
+    pair = Pair(wl)
+    pair.prefill(250)                   # 3 full chunks of 64 and a ragged chunk of 58
+    # 250 sequential fp32 IIR steps with |lambda| <= 0.99 accumulate rounding ~ eps/(1-|lambda|)
+    pair.compare_state(tol=5e-5)
+
+
+def test_tiny_fp32_rounds_greedy():
+    wl = get_workload("tiny_d64_fp32")
+    pair = Pair(wl)
+    pair.import_synthetic(wl.prefix_len)
+    assert _lockstep(pair, 6) <= 1
+    # identity drafter: every draft accepted, bonus from the last position
+    rnd = gen_round(wl, 100)
+    rnd["tokens"] = identity_drafts(pair, rnd)
+    res, gk, gc, _ = pair.run_round(rnd)
+    assert res.k[0] == wl.gamma and gk[0] == wl.gamma and gc[0] == res.corr[0]
+    pair.compare_state()
+
+
+@pytest.mark.parametrize("k_force", list(range(7)))
+def test_slice_at_every_k(k_force):
+    """State restoration at each block index (Lemma 3): FIR tail, IIR state, KV length."""
+    wl = get_workload("tiny_d64_fp32")
+    pair = Pair(wl)
+    pair.import_synthetic(40)
+    rnd = gen_round(wl, 7)
+    rnd["tokens"] = identity_drafts(pair, rnd, wrong_at=k_force if k_force < wl.gamma else None)
+    kv0 = pair.states[0].kv_len
+    res, gk, gc, _ = pair.run_round(rnd)
+    assert res.k[0] == k_force and gk[0] == k_force and gc[0] == res.corr[0]
+    assert pair.states[0].kv_len == kv0 + k_force + 1
+    pair.compare_state()
+    # decoding continues identically from the sliced state
+    assert _lockstep(pair, 2, first_round=8) <= 1
+
+
+def test_tiny_fp32_sampling_rounds():
+    wl = get_workload("tiny_d64_fp32").replace(mode="sampling", q_alpha=0.5)
+    pair = Pair(wl)
+    pair.import_synthetic(64)
+    assert _lockstep(pair, 10) <= 2
+
+
+def test_sampling_identity_drafts_with_q_equal_p_accept_all():
+    """With q = p (the target's own distribution), rejection sampling accepts every draft."""
+    wl = get_workload("tiny_d64_fp32").replace(mode="sampling", gamma=4)
+    pair = Pair(wl)
+    pair.import_synthetic(32)
+    rnd = gen_round(wl, 3)
+    toks = identity_drafts(pair, rnd)
+    probe = pair.states[0].clone()
+    q = np.zeros_like(rnd["q"])
+    for i in range(wl.gamma):
+        lg = pair.tgt.step(probe, int(toks[0, 0, i]))
+        p = np.exp(lg - lg.max())
+        q[0, 0, i] = (p / p.sum()).astype(np.float32)
+    rnd.update(tokens=toks, q=q)
+    res, gk, gc, _ = pair.run_round(rnd)
+    assert res.k[0] == wl.gamma and gk[0] == wl.gamma
+
+
+def test_multi_candidate_fp32():
+    wl = get_workload("tiny_d64_fp32").replace(batch=2, n_cand=3, gamma=5)
+    pair = Pair(wl)
+    pair.import_synthetic(48)
+    rnd = gen_round(wl, 1)
+    rnd["tokens"] = identity_drafts(pair, rnd, wrong_at=[1, 4, 2])
+    res, gk, gc, gcand = pair.run_round(rnd)
+    assert list(res.cand) == [1, 1] and list(gcand) == [1, 1]
+    np.testing.assert_array_equal(gk, [4, 4])
+    pair.compare_state()
+    assert _lockstep(pair, 3, first_round=2) <= 1
+
+
+def test_multi_candidate_sampling_bf16():
+    wl = get_workload("tiny_d64_fp32").replace(
+        d=256, dtype="bf16", head_dim=64, batch=2, n_cand=4, gamma=6, mode="sampling",
+        layers=(LayerSpec("fir", 3), LayerSpec("iir", 16), LayerSpec("fir", 7), LayerSpec("attn", 4)))
+    pair = Pair(wl)
+    pair.import_synthetic(300)
+    assert _lockstep(pair, 4) <= 2
+
+
+def test_bf16_small_stack_sampling():
+    wl = get_workload("d1024_l8_p8k_bf16").replace(d=256, head_dim=128, prefix_len=500,
+        layers=(LayerSpec("fir", 3), LayerSpec("iir", 16), LayerSpec("fir", 3), LayerSpec("attn", 2)) * 2)
+    pair = Pair(wl)
+    pair.prefill(wl.prefix_len)          # chunks of 128 and a ragged tail of 116
+    pair.compare_state(tol=TOL["bf16"])
+    assert _lockstep(pair, 5) <= 2
+
+
+def test_host_errors():
+    from lossless_speculative_verify_gb300 import EvsError
+    wl = get_workload("tiny_d64_fp32")
+    pair = Pair(wl, t_max=20)
+    with pytest.raises(EvsError) as e:
+        pair.ver.slice()
+    assert e.value.status == 3                              # slice without a verify
+    with pytest.raises(EvsError) as e:
+        pair.ver.prefill(torch.zeros((1, 21), dtype=torch.int32, device="cuda"))
+    assert e.value.status == 2                              # beyond t_max
+    pair.ver.prefill(torch.full((1, 14), 65, dtype=torch.int32, device="cuda"))
+    toks = torch.full((1, 1, 7), 65, dtype=torch.int32, device="cuda")
+    with pytest.raises(EvsError) as e:
+        pair.ver.verify(toks)                               # 14 + 7 > 20
+    assert e.value.status == 2
+    assert pair.ver.flags() == 0
+
+
+def test_device_flag_on_bad_token_and_bad_k():
+    wl = get_workload("tiny_d64_fp32")
+    pair = Pair(wl)
+    pair.import_synthetic(16)
+    toks = torch.full((1, 1, 7), 65, dtype=torch.int32, device="cuda")
+    toks[0, 0, 3] = 9999
+    pair.ver.verify(toks)
+    assert pair.ver.flags() & 8
+    bad_k = torch.full((1,), 99, dtype=torch.int32, device="cuda")
+    pair.ver.slice(bad_k)
+    assert pair.ver.flags() & 2
