@@ -318,7 +318,8 @@ __global__ void attn_combine_kernel(const float* __restrict__ Y, int ldy, const 
     const int c = qi / Tb, i = qi % Tb;
     const int e = threadIdx.x;
     const bool act = e < dh;
-    const int n = kv_base[b];
+    const int n = kv_base[b];  // rows n + j past t_max were never written (overflow flag set);
+                               // their reads are clamped to stay in bounds
     const int used = min((n + chunk - 1) / chunk, splits);  // splits that saw keys
     float M = -INFINITY;
     for (int s = 0; s < used; ++s) {
@@ -331,7 +332,7 @@ __global__ void attn_combine_kernel(const float* __restrict__ Y, int ldy, const 
     for (int j = 0; j <= i; ++j) {
         float kval = 0.f;
         if (act) {
-            kval = in_cache ? to_f32(kc[(((size_t)b * H + hh) * t_max + n + j) * dh + e])
+            kval = in_cache ? to_f32(kc[(((size_t)b * H + hh) * t_max + min(n + j, t_max - 1)) * dh + e])
                             : to_f32(ks[((((size_t)(b * C + c)) * H + hh) * Tb + j) * dh + e]);
         }
         const float sj = block_sum(qv * kval, red) * scale;
@@ -352,7 +353,7 @@ __global__ void attn_combine_kernel(const float* __restrict__ Y, int ldy, const 
         const float w = __expf(sc_blk[j] - M);
         L += w;
         if (act) {
-            const float vval = in_cache ? to_f32(vc[(((size_t)b * H + hh) * t_max + n + j) * dh + e])
+            const float vval = in_cache ? to_f32(vc[(((size_t)b * H + hh) * t_max + min(n + j, t_max - 1)) * dh + e])
                                         : to_f32(vs[((((size_t)(b * C + c)) * H + hh) * Tb + j) * dh + e]);
             O = fmaf(w, vval, O);
         }
