@@ -31,8 +31,8 @@ steps, acceptance, snapshot at k).
 from .model import Target, SeqState
 from .accept import (softmax_t, greedy_accept, sampling_accept, inverse_cdf, residual,
                      select_candidate)
-from .verify import verify_round, prefill, RoundResult
+from .verify import verify_round, prefill, RoundResult, block_pass, accept_block, commit
 
 __all__ = ["Target", "SeqState", "softmax_t", "greedy_accept", "sampling_accept",
            "inverse_cdf", "residual", "select_candidate", "verify_round", "prefill",
-           "RoundResult"]
+           "RoundResult", "block_pass", "accept_block", "commit"]

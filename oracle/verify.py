@@ -39,28 +39,25 @@ def prefill(target, state, tokens):
         target.step(state, int(x))
 
 
-def verify_round(target, states, tokens, q=None, u=None, mode="greedy", temperature=1.0,
-                 tau=0.0) -> RoundResult:
-    """``states`` is a list (one ``SeqState`` per sequence), updated in place to the
-    sliced state. tokens int [B, C, gamma+1]; q [B, C, gamma, V]; u [B, C, gamma+1]."""
+def block_pass(target, states, tokens):
+    """Decode every candidate's block one token at a time from the pre-round state and keep
+    the state after each position. ``states`` is left at the pre-round state. Returns a
+    dict with logits [B, C, T, V], per-position snapshots, the block K/V rows of each
+    candidate and the per-layer traces."""
     tokens = np.asarray(tokens)
     B, C, T = tokens.shape
-    g = T - 1
-    V = target.wl.vocab
-    res = RoundResult(logits=np.zeros((B, C, T, V)), k_c=np.zeros((B, C), np.int64),
-                      corr_c=np.zeros((B, C), np.int64), tie_c=np.zeros((B, C), bool),
-                      k=np.zeros(B, np.int64), corr=np.zeros(B, np.int64),
-                      cand=np.zeros(B, np.int64), tie=np.zeros(B, bool))
+    out = {"logits": np.zeros((B, C, T, target.wl.vocab)), "base": [], "snaps": [], "rows": [],
+           "traces": []}
     for b in range(B):
         st = states[b]
         base = st.snapshot()
         snaps_c, rows_c, traces_b = [], [], []
         for c in range(C):
             st.restore(base)
-            snaps, logits, traces = [], [], []
+            snaps, traces = [], []
             for i in range(T):
                 tr = []
-                logits.append(target.step(st, int(tokens[b, c, i]), tr))
+                out["logits"][b, c, i] = target.step(st, int(tokens[b, c, i]), tr)
                 traces.append(tr)
                 snaps.append(st.snapshot())
             rows = []
@@ -69,29 +66,64 @@ def verify_round(target, states, tokens, q=None, u=None, mode="greedy", temperat
                     n0 = L["kv"].length - T
                     rows.append((n0, L["kv"].k[:, n0:n0 + T].copy(),
                                  L["kv"].v[:, n0:n0 + T].copy()))
-            logits = np.asarray(logits)
-            p = softmax_t(logits, temperature)
-            if mode == "greedy":
-                k, corr, tie = greedy_accept(p, tokens[b, c, 1:], logits, tau)
-            else:
-                k, corr, tie, _ = sampling_accept(p, q[b, c], tokens[b, c, 1:], u[b, c], tau)
-            res.logits[b, c] = logits
-            res.k_c[b, c], res.corr_c[b, c], res.tie_c[b, c] = k, corr, tie
             snaps_c.append(snaps)
             rows_c.append(rows)
             traces_b.append(traces)
-        cb = select_candidate(res.k_c[b])
-        kb = int(res.k_c[b, cb])
-        # commit: the chosen candidate's block K/V rows become the cache rows after the
-        # prefix, then the state returns to its snapshot at block index k
-        it = iter(rows_c[cb])
+        st.restore(base)
+        out["base"].append(base)
+        out["snaps"].append(snaps_c)
+        out["rows"].append(rows_c)
+        out["traces"].append(traces_b)
+    return out
+
+
+def accept_block(logits, tokens, q=None, u=None, mode="greedy", temperature=1.0, tau=0.0):
+    """Acceptance for every (sequence, candidate) of a block from its logits [B, C, T, V];
+    returns k_c, corr_c, tie_c [B, C] and the committed k, corr, cand, tie [B]."""
+    tokens = np.asarray(tokens)
+    B, C, T = tokens.shape
+    k_c = np.zeros((B, C), np.int64)
+    corr_c = np.zeros((B, C), np.int64)
+    tie_c = np.zeros((B, C), bool)
+    for b in range(B):
+        for c in range(C):
+            lg = np.asarray(logits[b, c], np.float64)
+            p = softmax_t(lg, temperature)
+            if mode == "greedy":
+                k, corr, tie = greedy_accept(p, tokens[b, c, 1:], lg, tau)
+            else:
+                k, corr, tie, _ = sampling_accept(p, q[b, c], tokens[b, c, 1:], u[b, c], tau)
+            k_c[b, c], corr_c[b, c], tie_c[b, c] = k, corr, tie
+    cand = np.array([select_candidate(k_c[b]) for b in range(B)], np.int64)
+    k = k_c[np.arange(B), cand]
+    corr = corr_c[np.arange(B), cand]
+    return k_c, corr_c, tie_c, k, corr, cand, tie_c.any(axis=1)
+
+
+def commit(states, bp, k, cand):
+    """State slicing at block index k[b] of candidate cand[b]: the chosen candidate's block
+    K/V rows become the cache rows after the prefix, then each sequence returns to its
+    snapshot at k (readable KV length advanced by k+1, FIR tail and IIR state at k)."""
+    for b, st in enumerate(states):
+        cb, kb = int(cand[b]), int(k[b])
+        st.restore(bp["base"][b])
+        it = iter(bp["rows"][b][cb])
         for L in st.layers:
             if L["kind"] == "attn":
                 n0, kr, vr = next(it)
+                T = kr.shape[1]
                 L["kv"].k[:, n0:n0 + T] = kr
                 L["kv"].v[:, n0:n0 + T] = vr
-        st.restore(snaps_c[cb][kb])
-        res.k[b], res.corr[b], res.cand[b] = kb, res.corr_c[b, cb], cb
-        res.tie[b] = bool(res.tie_c[b].any())
-        res.traces.append(traces_b)
-    return res
+        st.restore(bp["snaps"][b][cb][kb])
+
+
+def verify_round(target, states, tokens, q=None, u=None, mode="greedy", temperature=1.0,
+                 tau=0.0) -> RoundResult:
+    """``states`` is a list (one ``SeqState`` per sequence), updated in place to the
+    sliced state. tokens int [B, C, gamma+1]; q [B, C, gamma, V]; u [B, C, gamma+1]."""
+    bp = block_pass(target, states, tokens)
+    k_c, corr_c, tie_c, k, corr, cand, tie = accept_block(bp["logits"], tokens, q, u, mode,
+                                                          temperature, tau)
+    commit(states, bp, k, cand)
+    return RoundResult(logits=bp["logits"], k_c=k_c, corr_c=corr_c, tie_c=tie_c, k=k, corr=corr,
+                       cand=cand, tie=tie, traces=bp["traces"])

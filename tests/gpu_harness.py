@@ -34,6 +34,20 @@ def make_verifier(wl, weights, t_max, near_tie_tau=None):
     return Verifier(cfg, dw)
 
 
+class RoundOut:
+    """own / kern: oracle decisions (k_c, corr_c, tie_c, k, corr, cand, tie) from its own
+    fp64 logits and from the library's fp32 logits; gk, gc, gcand: the library's."""
+
+    def __init__(self, own, kern, gk, gc, gcand, bp):
+        self.own, self.kern, self.gk, self.gc, self.gcand, self.bp = own, kern, gk, gc, gcand, bp
+        self.k, self.corr, self.cand, self.tie = own[3], own[4], own[5], own[6]
+
+
+class _Res:
+    def __init__(self, bp):
+        self.logits, self.traces = bp["logits"], bp["traces"]
+
+
 class Pair:
     """Oracle and library driven in lockstep."""
 
@@ -110,27 +124,45 @@ class Pair:
         return rnd
 
     def run_round(self, rnd, check_block=True, tol=None):
-        """Verify + slice on both sides from the current (identical) state. Returns
-        (oracle result, gpu k, gpu corr, gpu cand, near_tie_oracle)."""
+        """Verify + slice on both sides from the current (identical) state.
+
+        Decisions are checked in two ways: (1) the oracle's acceptance applied to the
+        library's fp32 logits (the kernel's precision) must give exactly the library's k,
+        correction and candidate unless a near-tie at fp32 resolution (tau 1e-5) is flagged;
+        (2) the oracle's own fp64 decisions are returned for callers that compare them too.
+        The oracle then commits the state at the library's (k, candidate), so both sides stay
+        in lockstep and every slice is compared exactly."""
         wl = self.wl
         tol = TOL[wl.dtype] if tol is None else tol
-        tau = TAU[wl.dtype]
         dev = lambda a, dt: torch.as_tensor(a, dtype=dt).cuda().contiguous()
         toks = dev(rnd["tokens"], torch.int32)
-        q = dev(rnd["q"], torch.float32) if wl.mode == "sampling" else None
-        u = dev(rnd["u"], torch.float32) if wl.mode == "sampling" else None
-        pre = [s.snapshot() for s in self.states]
-        res = oracle.verify_round(self.tgt, self.states, rnd["tokens"], rnd["q"], rnd["u"], wl.mode,
-                                  wl.temperature, tau)
+        sampling = wl.mode == "sampling"
+        q = dev(rnd["q"], torch.float32) if sampling else None
+        u = dev(rnd["u"], torch.float32) if sampling else None
+        bp = oracle.block_pass(self.tgt, self.states, rnd["tokens"])
+        own = oracle.accept_block(bp["logits"], rnd["tokens"], rnd["q"], rnd["u"], wl.mode,
+                                  wl.temperature, TAU[wl.dtype])
         k, corr, cand, tie = self.ver.verify(toks, q, u)
         torch.cuda.synchronize()
         if check_block:
-            self.check_block(res, tol)
+            self.check_block(bp, tol)
+        B, C, T, V = wl.batch, wl.n_cand, wl.block, wl.vocab
+        glog = self.ver.buffer(0, -1, torch.float32, (B, C, T, V)).cpu().numpy()
+        kern = oracle.accept_block(glog, rnd["tokens"], rnd["q"], rnd["u"], wl.mode,
+                                   wl.temperature, TAU["f32"])
         gk, gc, gcand = k.cpu().numpy(), corr.cpu().numpy(), cand.cpu().numpy()
+        gcand = gcand if C > 1 else np.zeros_like(gk)
+        for b in range(B):
+            if kern[6][b]:
+                continue
+            assert gk[b] == kern[3][b] and gc[b] == kern[4][b] and gcand[b] == kern[5][b], \
+                (b, gk, gc, gcand, kern[3:6])
+        oracle.commit(self.states, bp, gk, gcand)
         self.ver.slice(k, cand)
-        return res, gk, gc, gcand
+        return RoundOut(own, kern, gk, gc, gcand, bp)
 
     def check_block(self, res, tol):
+        res = _Res(res)
         """Block forward outputs: logits, retained IIR states, FIR inputs, block K/V."""
         wl = self.wl
         B, C, T, V, d = wl.batch, wl.n_cand, wl.block, wl.vocab, wl.d
