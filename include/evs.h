@@ -69,7 +69,8 @@ enum {
     EVS_FLAG_KV_OVERFLOW = 1u,    /* a write past t_max was skipped                     */
     EVS_FLAG_BAD_K = 2u,          /* slice saw k outside [0, gamma] or a bad candidate  */
     EVS_FLAG_EMPTY_RESIDUAL = 4u, /* max(0, p - q) summed to 0 in fp32; p was used      */
-    EVS_FLAG_BAD_TOKEN = 8u       /* a token id outside [0, vocab) was clamped          */
+    EVS_FLAG_BAD_TOKEN = 8u,      /* a token id outside [0, vocab) was clamped          */
+    EVS_FLAG_TIMEOUT = 16u        /* a kernel gave up a bounded wait; its output is void */
 };
 
 #define EVS_MAX_LAYERS 64
@@ -237,6 +238,14 @@ evs_status evs_profile_read(evs_handle* h, int32_t* launches, float* ms, int32_t
 
 /* Number of kernel launches the last public call enqueued (for accounting). */
 int32_t evs_last_launch_count(evs_handle* h);
+
+/* Diagnostics: Y[m][n] (+)= sum_k X[m][k] W[n][k] with the library's projection kernel
+ * (the same launch path the block forward uses). X: device bf16 [x_rows][K] (x_rows >= M),
+ * W: device bf16 out-major [N][K], Y: device fp32 [M][ldy]. Uses the handle's stream and
+ * split-K scratch; needs a bf16 handle, M <= 512, N % 128 == 0, K % 64 == 0, K <= d and
+ * N <= max(3d, vocab). EVS_ERR_INVALID_ARG otherwise. */
+evs_status evs_debug_projection(evs_handle* h, const void* X, int32_t x_rows, const void* W, float* Y,
+                                int32_t M, int32_t N, int32_t K, int32_t ldy, int32_t accumulate);
 
 /* Static description of a status code. */
 const char* evs_status_str(evs_status s);

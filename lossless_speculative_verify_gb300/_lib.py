@@ -17,7 +17,7 @@ EVS_OK, EVS_ERR_INVALID_ARG, EVS_ERR_CAPACITY, EVS_ERR_STATE, EVS_ERR_CUDA = ran
 LAYER_FIR, LAYER_IIR, LAYER_ATTN = 0, 1, 2
 DTYPE_F32, DTYPE_BF16 = 0, 1
 MODE_GREEDY, MODE_SAMPLING = 0, 1
-FLAG_KV_OVERFLOW, FLAG_BAD_K, FLAG_EMPTY_RESIDUAL, FLAG_BAD_TOKEN = 1, 2, 4, 8
+FLAG_KV_OVERFLOW, FLAG_BAD_K, FLAG_EMPTY_RESIDUAL, FLAG_BAD_TOKEN, FLAG_TIMEOUT = 1, 2, 4, 8, 16
 (BUF_LOGITS, BUF_FIR_STAGE, BUF_IIR_RET, BUF_K_CACHE, BUF_V_CACHE, BUF_K_SIDE, BUF_V_SIDE,
  BUF_KV_LEN, BUF_FIR_TAIL, BUF_IIR_STATE, BUF_CAND_K, BUF_CAND_CORR) = range(12)
 
@@ -25,7 +25,7 @@ EXPORTED = (
     "evs_workspace_bytes", "evs_create", "evs_destroy", "evs_set_stream", "evs_reset",
     "evs_prefill", "evs_verify_block", "evs_slice_state", "evs_import_state",
     "evs_export_state", "evs_debug_buffer", "evs_device_flags", "evs_last_launch_count",
-    "evs_status_str", "evs_profile_enable", "evs_profile_read",
+    "evs_status_str", "evs_profile_enable", "evs_profile_read", "evs_debug_projection",
 )
 KERNEL_KINDS = ("embed", "norm", "gemm", "fir", "iir", "kv_write", "attn", "attn_combine", "accept",
                 "slice", "advance")
@@ -106,6 +106,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.evs_profile_enable.argtypes = [vp, i32]
     lib.evs_profile_read.restype = C.c_int
     lib.evs_profile_read.argtypes = [vp, C.POINTER(i32), C.POINTER(C.c_float), i32]
+    lib.evs_debug_projection.restype = C.c_int
+    lib.evs_debug_projection.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, i32, i32]
     lib.evs_status_str.restype = C.c_char_p
     lib.evs_status_str.argtypes = [C.c_int]
     _lib = lib

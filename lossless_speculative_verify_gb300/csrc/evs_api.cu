@@ -83,7 +83,7 @@ bool valid_config(const evs_config* c) {
     if (c->batch < 1 || c->batch > 64 || c->n_cand < 1 || c->n_cand > 16) return false;
     if ((long long)c->batch * c->n_cand * (c->gamma + 1) > 512) return false;
     if (c->prefill_chunk < 1 || c->prefill_chunk > 128) return false;
-    if ((long long)c->batch * c->prefill_chunk > 1024) return false;
+    if ((long long)c->batch * c->prefill_chunk > 512) return false;
     if (c->t_max < 1) return false;
     if (c->dtype != EVS_DTYPE_F32 && c->dtype != EVS_DTYPE_BF16) return false;
     if (c->mode != EVS_MODE_GREEDY && c->mode != EVS_MODE_SAMPLING) return false;
@@ -178,12 +178,16 @@ size_t carve(const evs_config& c, char* base, evs_handle* h) {
     char* y = take((size_t)g.M_max * 3 * d * 4);
     char* logits = take((size_t)g.M_verify * c.vocab * 4);
     char* part = take(B * (size_t)g.h_max * g.kv_splits * g.q_max * (dh + 2) * 4);
+    char* gpart = take((size_t)152 * 128 * g.M_max * 4);
+    char* gcnt = take((size_t)(std::max(3 * c.d, c.vocab) / 128 + 1) * 4);
     if (h) {
         h->h = (float*)hbuf;
         h->act = act;
         h->y = (float*)y;
         h->logits = (float*)logits;
         h->attn_part = (float*)part;
+        h->gemm_part = (float*)gpart;
+        h->gemm_counters = (int*)gcnt;
         h->g = g;
     }
     return off;
@@ -292,6 +296,9 @@ evs_status evs_create(const evs_config* cfg, const evs_weights* weights, void* w
     evs_status st = cuda_ok(cudaMemcpyAsync(h->layer_dev, h->layer, sizeof(evs::LayerDesc) * cfg->n_layers,
                                             cudaMemcpyHostToDevice, h->stream));
     if (st == EVS_OK) st = cuda_ok(cudaMemsetAsync(h->flags, 0, 4, h->stream));
+    if (st == EVS_OK)
+        st = cuda_ok(cudaMemsetAsync(h->gemm_counters, 0, (std::max(3 * cfg->d, cfg->vocab) / 128 + 1) * 4,
+                                     h->stream));
     if (st == EVS_OK) st = zero_state(h);
     if (st == EVS_OK) st = cuda_ok(cudaStreamSynchronize(h->stream));  // layer table copied from host
     if (st != EVS_OK) {
@@ -521,6 +528,18 @@ evs_status evs_device_flags(evs_handle* h, uint32_t* flags, int32_t clear) {
 }
 
 int32_t evs_last_launch_count(evs_handle* h) { return h ? h->launches : 0; }
+
+evs_status evs_debug_projection(evs_handle* h, const void* X, int32_t x_rows, const void* W, float* Y, int32_t M,
+                                int32_t N, int32_t K, int32_t ldy, int32_t accumulate) {
+    if (!h || !X || !W || !Y || h->cfg.dtype != EVS_DTYPE_BF16) return EVS_ERR_INVALID_ARG;
+    if (!evs::gemm_tc_supported(M, N, K) || x_rows < M || K > h->cfg.d || ldy < N ||
+        N > std::max(3 * h->cfg.d, h->cfg.vocab) || M > h->g.M_max)
+        return EVS_ERR_INVALID_ARG;
+    h->launches = 0;
+    if (!evs::launch_gemm_tc(h, X, x_rows, W, Y, M, N, K, ldy, accumulate)) return EVS_ERR_CUDA;
+    h->launches = 1;
+    return after_launch(h);
+}
 
 const char* evs_status_str(evs_status s) {
     switch (s) {

@@ -62,6 +62,8 @@ struct evs_handle {
     float* y;             // [M_max][3d] projection outputs
     float* logits;        // [M_verify][vocab]
     float* attn_part;     // [B][H_max][splits][q_max][dh + 2]
+    float* gemm_part;     // split-K partial sums [<= 152 * 128 * M_max] fp32
+    int* gemm_counters;   // [max(3d, vocab) / 128] split-K arrival counters
     evs::LayerDesc layer[EVS_MAX_LAYERS];
     evs::LayerDesc* layer_dev;   // device copy
     // sizes of per-layer buffers (bytes), for evs_debug_buffer
@@ -87,6 +89,10 @@ void launch_embed(evs_handle* h, const int32_t* tokens, int tok_stride_bc, const
 void launch_rmsnorm(evs_handle* h, const Pass& p);
 void launch_gemm(evs_handle* h, const void* A, const void* W, float* Y, int M, int N, int K,
                  int ldy, int accumulate);
+// tcgen05 projection (gemm_tc.cu); false when it cannot take the shape
+bool gemm_tc_supported(int M, int N, int K);
+bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, float* Y, int M, int N,
+                    int K, int ldy, int accumulate);
 void launch_fir(evs_handle* h, int layer, const Pass& p);
 void launch_iir(evs_handle* h, int layer, const Pass& p);
 void launch_kv_write(evs_handle* h, int layer, const Pass& p);

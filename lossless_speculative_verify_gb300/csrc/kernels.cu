@@ -682,6 +682,12 @@ void launch_rmsnorm(evs_handle* h, const Pass& p) {
 void launch_gemm(evs_handle* h, const void* A, const void* W, float* Y, int M, int N, int K, int ldy,
                  int accumulate) {
     prof_begin(h, EVS_K_GEMM);
+    if (is_bf16(h) && gemm_tc_supported(M, N, K) &&
+        launch_gemm_tc(h, A, h->g.M_max, W, Y, M, N, K, ldy, accumulate)) {
+        h->launches++;
+        prof_end(h, EVS_K_GEMM);
+        return;
+    }
     dim3 grid((N + GS_BN - 1) / GS_BN, (M + GS_BM - 1) / GS_BM);
     if (is_bf16(h))
         gemm_simt_kernel<bf16><<<grid, 256, 0, h->stream>>>((const bf16*)A, (const bf16*)W, Y, M, N, K, ldy,
