@@ -293,6 +293,14 @@ evs_status evs_create(const evs_config* cfg, const evs_weights* weights, void* w
     h->ws = (char*)workspace;
     h->ws_bytes = ws_bytes;
     carve(*cfg, h->ws, h);
+    h->tc_smem_max = 0;
+    if (cfg->dtype == EVS_DTYPE_BF16) {
+        h->tc_smem_max = evs::gemm_tc_init();
+        if (h->tc_smem_max < 0) {
+            free(h);
+            return EVS_ERR_CUDA;
+        }
+    }
     evs_status st = cuda_ok(cudaMemcpyAsync(h->layer_dev, h->layer, sizeof(evs::LayerDesc) * cfg->n_layers,
                                             cudaMemcpyHostToDevice, h->stream));
     if (st == EVS_OK) st = cuda_ok(cudaMemsetAsync(h->flags, 0, 4, h->stream));

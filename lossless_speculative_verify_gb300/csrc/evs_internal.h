@@ -64,6 +64,7 @@ struct evs_handle {
     float* attn_part;     // [B][H_max][splits][q_max][dh + 2]
     float* gemm_part;     // split-K partial sums [<= 152 * 128 * M_max] fp32
     int* gemm_counters;   // [max(3d, vocab) / 128] split-K arrival counters
+    int tc_smem_max;      // dynamic shared memory the projection kernel may use (bytes)
     evs::LayerDesc layer[EVS_MAX_LAYERS];
     evs::LayerDesc* layer_dev;   // device copy
     // sizes of per-layer buffers (bytes), for evs_debug_buffer
@@ -91,6 +92,7 @@ void launch_gemm(evs_handle* h, const void* A, const void* W, float* Y, int M, i
                  int ldy, int accumulate);
 // tcgen05 projection (gemm_tc.cu); false when it cannot take the shape
 bool gemm_tc_supported(int M, int N, int K);
+int gemm_tc_init();
 bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, float* Y, int M, int N,
                     int K, int ldy, int accumulate);
 void launch_fir(evs_handle* h, int layer, const Pass& p);

@@ -199,6 +199,21 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Opt the kernel into the largest dynamic shared memory the device allows next to its
+// static shared memory; returns that size in bytes, or -1 on failure.
+int gemm_tc_init() {
+    int dev = 0, optin = 0;
+    cudaFuncAttributes fa;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, gemm_tc_kernel) != cudaSuccess)
+        return -1;
+    const int dyn = optin - (int)fa.sharedSizeBytes;
+    if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn) != cudaSuccess)
+        return -1;
+    return dyn;
+}
+
 int tc_splits(int N, int K) {
     const int tiles = N / TC_BM, kblocks = K / TC_BK;
     int s = 152 / tiles;
@@ -229,11 +244,7 @@ bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, flo
     int ncols = 32;
     while (ncols < n_pad) ncols <<= 1;
     const size_t smem = (size_t)stages * stage_bytes + 1024 + (2 * stages + 1) * 8;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        attr_set = true;
-    }
+    if ((int)smem > h->tc_smem_max) return false;
     TcArgs a{Y, ldy, M, N, kblocks, splits, n_pad, stages, accumulate, ncols, h->gemm_part, h->gemm_counters,
              h->flags};
     gemm_tc_kernel<<<dim3(tiles, splits), 128, smem, h->stream>>>(ta, tb, a);
