@@ -247,6 +247,28 @@ int32_t evs_last_launch_count(evs_handle* h);
 evs_status evs_debug_projection(evs_handle* h, const void* X, int32_t x_rows, const void* W, float* Y,
                                 int32_t M, int32_t N, int32_t K, int32_t ldy, int32_t accumulate);
 
+/* Projection for callers that cannot allocate device memory: no handle, no workspace,
+ * no cudaMalloc / cudaFree or allocating library call. The pages have no counterpart of
+ * this entry point; it exists for hosts that own all device memory and forbid allocation
+ * while they execute (plugin-style engines), and for latency-critical loops where an
+ * allocation would synchronise the device.
+ * Computes Y[m][n] (+)= sum_k X[m][k] W[n][k] with the same tcgen05 kernel as
+ * evs_debug_projection. X: device bf16 [x_rows][K] (x_rows >= M); W: device bf16
+ * out-major [N][K]; Y: device fp32 [M][ldy]; stream: a cudaStream_t. Needs M <= 512,
+ * N % 128 == 0, N <= 32768, K % 64 == 0.
+ * Scratch: one fixed array of 8 MiB of fp32 partial sums (plus 256 counters) compiled
+ * into the library, held on every GPU that loads it until the process exits. Shapes whose
+ * split-K partial sums (splits x M x N floats) exceed 2^21 floats return EVS_ERR_CAPACITY.
+ * The first call on a device looks up the array's device address and sets the kernel's
+ * shared-memory limit for that device; make that first call before any stream capture.
+ * Every call reuses the same array and finds the previous call's contents there; the
+ * counters are cleared on the stream at each call. Calls that overlap on the GPU (issued
+ * on different streams, or from several host threads) race on it: order them on one
+ * stream. EVS_ERR_INVALID_ARG for bad shapes or pointers, EVS_ERR_CUDA if a
+ * CUDA call fails. */
+evs_status evs_projection_noalloc(const void* X, int32_t x_rows, const void* W, float* Y, int32_t M,
+                                  int32_t N, int32_t K, int32_t ldy, int32_t accumulate, void* stream);
+
 /* Static description of a status code. */
 const char* evs_status_str(evs_status s);
 

@@ -252,3 +252,74 @@ bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, flo
 }
 
 }  // namespace evs
+
+// ---- projection without any allocation ------------------------------------------------------
+// Same kernel, with its split-K scratch (partial sums, arrival counters, flag word) in one
+// file-scope device array instead of a caller workspace. The array is fixed in size and
+// resident on every GPU that loads the library until the process exits.
+namespace evs {
+namespace {
+
+constexpr size_t kNoAllocPartFloats = (size_t)2 << 20;   // 8 MiB of fp32 partial sums
+constexpr int kNoAllocCounters = 256;                    // 128-channel tiles: N <= 32768
+constexpr int kNoAllocMaxDevices = 64;
+
+struct NoAllocScratch {
+    float part[kNoAllocPartFloats];
+    int counters[kNoAllocCounters];
+    uint32_t flags;
+};
+
+static __device__ __align__(256) NoAllocScratch g_noalloc_scratch;
+
+// Per-device set-up results: the array's device address and the kernel's shared-memory
+// limit. Filled by the first call on each device.
+NoAllocScratch* g_noalloc_ptr[kNoAllocMaxDevices];
+int g_noalloc_smem[kNoAllocMaxDevices];
+
+}  // namespace
+}  // namespace evs
+
+extern "C" evs_status evs_projection_noalloc(const void* X, int32_t x_rows, const void* W, float* Y, int32_t M,
+                                             int32_t N, int32_t K, int32_t ldy, int32_t accumulate,
+                                             void* stream) {
+    using namespace evs;
+    if (!X || !W || !Y || !gemm_tc_supported(M, N, K) || x_rows < M || ldy < N || N / TC_BM > kNoAllocCounters)
+        return EVS_ERR_INVALID_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return EVS_ERR_CUDA;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return EVS_ERR_INVALID_ARG;
+    if (!g_noalloc_ptr[dev]) {
+        // one-time set-up on this device (the device is current here)
+        NoAllocScratch* p = nullptr;
+        if (cudaGetSymbolAddress((void**)&p, g_noalloc_scratch) != cudaSuccess || !p) return EVS_ERR_CUDA;
+        const int smem_max = gemm_tc_init();
+        if (smem_max < 0) return EVS_ERR_CUDA;
+        g_noalloc_smem[dev] = smem_max;
+        g_noalloc_ptr[dev] = p;
+    }
+    NoAllocScratch* sc = g_noalloc_ptr[dev];
+    const int splits = tc_splits(N, K);
+    if (splits > 1 && (size_t)splits * M * N > kNoAllocPartFloats) return EVS_ERR_CAPACITY;
+    const int n_pad = M > 256 ? 512 : (M + 15) / 16 * 16;
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, W, (uint64_t)N, (uint64_t)K, TC_BM)) return EVS_ERR_CUDA;
+    if (!make_map(&tb, X, (uint64_t)x_rows, (uint64_t)K, (uint32_t)(n_pad < 256 ? n_pad : 256))) return EVS_ERR_CUDA;
+    const int tiles = N / TC_BM, kblocks = K / TC_BK;
+    const int per = (kblocks + splits - 1) / splits;
+    const int stage_bytes = TC_A_BYTES + n_pad * 128;
+    int stages = TC_SMEM_BUDGET / stage_bytes;
+    if (stages > per) stages = per;
+    if (stages < 1) stages = 1;
+    int ncols = 32;
+    while (ncols < n_pad) ncols <<= 1;
+    const size_t smem = (size_t)stages * stage_bytes + 1024 + (2 * stages + 1) * 8;
+    if ((int)smem > g_noalloc_smem[dev]) return EVS_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    // the array keeps the previous call's contents: the counters must start at zero
+    if (cudaMemsetAsync(sc->counters, 0, sizeof(sc->counters), s) != cudaSuccess) return EVS_ERR_CUDA;
+    TcArgs a{Y, ldy, M, N, kblocks, splits, n_pad, stages, accumulate, ncols, sc->part, sc->counters, &sc->flags};
+    gemm_tc_kernel<<<dim3(tiles, splits), 128, smem, s>>>(ta, tb, a);
+    return cudaGetLastError() == cudaSuccess ? EVS_OK : EVS_ERR_CUDA;
+}
+
