@@ -177,7 +177,15 @@ size_t carve(const evs_config& c, char* base, evs_handle* h) {
     char* act = take((size_t)g.M_max * d * es);
     char* y = take((size_t)g.M_max * 3 * d * 4);
     char* logits = take((size_t)g.M_verify * c.vocab * 4);
-    char* part = take(B * (size_t)g.h_max * g.kv_splits * g.q_max * (dh + 2) * 4);
+    size_t splits_max = g.kv_splits;
+    if (c.dtype == EVS_DTYPE_BF16 && c.head_dim == 128) {
+        // the tensor-core attention may chunk the prefix more finely (its plan depends only
+        // on the pass shape and t_max; 200 KiB stands in for the shared-memory limit here)
+        const evs::AttnPlan pv = evs::attn_tc_plan(g.C * g.T, g.B, g.h_max, c.t_max, 200 * 1024);
+        const evs::AttnPlan pp = evs::attn_tc_plan(c.prefill_chunk, g.B, g.h_max, c.t_max, 200 * 1024);
+        splits_max = std::max(splits_max, (size_t)std::max(pv.splits, pp.splits));
+    }
+    char* part = take(B * (size_t)g.h_max * splits_max * g.q_max * (dh + 2) * 4);
     char* gpart = take((size_t)152 * 128 * g.M_max * 4);
     char* gcnt = take((size_t)(std::max(3 * c.d, c.vocab) / 128 + 1) * 4);
     if (h) {
@@ -296,9 +304,16 @@ evs_status evs_create(const evs_config* cfg, const evs_weights* weights, void* w
     h->tc_smem_max = 0;
     if (cfg->dtype == EVS_DTYPE_BF16) {
         h->tc_smem_max = evs::gemm_tc_init();
-        if (h->tc_smem_max < 0) {
+        const int attn_smem = evs::attn_tc_init();
+        if (h->tc_smem_max < 0 || attn_smem < 0) {
             free(h);
             return EVS_ERR_CUDA;
+        }
+        if (cfg->head_dim == 128) {
+            // plans use at most 200 KiB, the bound the partial buffer was sized with
+            const int sm = std::min(attn_smem, 200 * 1024);
+            h->plan_verify = evs::attn_tc_plan(h->g.C * h->g.T, h->g.B, h->g.h_max, cfg->t_max, sm);
+            h->plan_prefill = evs::attn_tc_plan(cfg->prefill_chunk, h->g.B, h->g.h_max, cfg->t_max, sm);
         }
     }
     evs_status st = cuda_ok(cudaMemcpyAsync(h->layer_dev, h->layer, sizeof(evs::LayerDesc) * cfg->n_layers,
@@ -308,6 +323,12 @@ evs_status evs_create(const evs_config* cfg, const evs_weights* weights, void* w
         st = cuda_ok(cudaMemsetAsync(h->gemm_counters, 0, (std::max(3 * cfg->d, cfg->vocab) / 128 + 1) * 4,
                                      h->stream));
     if (st == EVS_OK) st = zero_state(h);
+    for (int i = 0; i < cfg->n_layers && st == EVS_OK; ++i) {
+        // never-written cache rows are read (and multiplied by zero weights) at chunk edges
+        if (h->layer[i].kind != EVS_LAYER_ATTN) continue;
+        st = cuda_ok(cudaMemsetAsync(h->layer[i].kc, 0, h->cache_bytes[i], h->stream));
+        if (st == EVS_OK) st = cuda_ok(cudaMemsetAsync(h->layer[i].vc, 0, h->cache_bytes[i], h->stream));
+    }
     if (st == EVS_OK) st = cuda_ok(cudaStreamSynchronize(h->stream));  // layer table copied from host
     if (st != EVS_OK) {
         free(h);

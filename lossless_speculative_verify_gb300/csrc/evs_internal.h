@@ -32,6 +32,17 @@ struct Geometry {
     int kv_splits;    // ceil(t_max / kv_chunk)
 };
 
+// Prefix chunking of the tensor-core attention for one pass shape (attn_tc.cu).
+struct AttnPlan {
+    int ok;          // 1 if the tensor-core kernel takes this pass
+    int n_q;         // queries padded to 16 (MMA N)
+    int tiles;       // 128-key tiles per CTA
+    int splits;      // chunks covering t_max keys
+    int stages;      // TMA ring depth (32 KiB stages)
+    int ncols;       // TMEM columns
+    int smem;        // dynamic shared memory bytes
+};
+
 // A pass runs B sequences x C candidates x T block positions; row m = (b*C + c)*T + i.
 struct Pass {
     int B, C, T;        // sequences, candidates, positions per candidate
@@ -65,6 +76,7 @@ struct evs_handle {
     float* gemm_part;     // split-K partial sums [<= 152 * 128 * M_max] fp32
     int* gemm_counters;   // [max(3d, vocab) / 128] split-K arrival counters
     int tc_smem_max;      // dynamic shared memory the projection kernel may use (bytes)
+    evs::AttnPlan plan_verify, plan_prefill;   // tensor-core attention chunking per pass
     evs::LayerDesc layer[EVS_MAX_LAYERS];
     evs::LayerDesc* layer_dev;   // device copy
     // sizes of per-layer buffers (bytes), for evs_debug_buffer
@@ -93,6 +105,10 @@ void launch_gemm(evs_handle* h, const void* A, const void* W, float* Y, int M, i
 // tcgen05 projection (gemm_tc.cu); false when it cannot take the shape
 bool gemm_tc_supported(int M, int N, int K);
 int gemm_tc_init();
+// tcgen05 attention (attn_tc.cu)
+AttnPlan attn_tc_plan(int Q, int B, int H, int t_max, int smem_max);
+int attn_tc_init();
+bool launch_attn_tc(evs_handle* h, int layer, const Pass& p, const AttnPlan& plan);
 bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, float* Y, int M, int N,
                     int K, int ldy, int accumulate);
 void launch_fir(evs_handle* h, int layer, const Pass& p);

@@ -757,6 +757,12 @@ void launch_attention(evs_handle* h, int li, const Pass& p) {
     const int H = L.param, dh = h->cfg.head_dim;
     const int Q = p.C * p.T;
     const Geometry& g = h->g;
+    const AttnPlan& plan = p.commit ? h->plan_prefill : h->plan_verify;
+    int splits = g.kv_splits, chunk = g.kv_chunk;
+    if (plan.ok && launch_attn_tc(h, li, p, plan)) {
+        splits = plan.splits;
+        chunk = plan.tiles * 128;
+    } else {
     dim3 grid(g.kv_splits, p.B * H, (Q + AQ - 1) / AQ);
     if (is_bf16(h))
         attn_split_kernel<bf16><<<grid, 256, 0, h->stream>>>(h->y, 3 * d, (const bf16*)L.kc, (const bf16*)L.vc,
@@ -765,6 +771,7 @@ void launch_attention(evs_handle* h, int li, const Pass& p) {
         attn_split_kernel<float><<<grid, 256, 0, h->stream>>>(h->y, 3 * d, (const float*)L.kc,
             (const float*)L.vc, H, dh, Q, g.q_max, h->cfg.t_max, g.kv_chunk, g.kv_splits, h->kv_base,
             h->attn_part);
+    }
     h->launches++;
     prof_end(h, EVS_K_ATTN);
     prof_begin(h, EVS_K_ATTN_COMBINE);
@@ -773,11 +780,11 @@ void launch_attention(evs_handle* h, int li, const Pass& p) {
     if (is_bf16(h))
         attn_combine_kernel<bf16><<<grid2, thr, 0, h->stream>>>(h->y, 3 * d, (const bf16*)L.kc,
             (const bf16*)L.vc, (const bf16*)L.ks, (const bf16*)L.vs, H, dh, p.C, p.T, Q, g.q_max, h->cfg.t_max,
-            g.kv_splits, g.kv_chunk, p.kv_in_cache, h->kv_base, h->attn_part, (bf16*)h->act, d);
+            splits, chunk, p.kv_in_cache, h->kv_base, h->attn_part, (bf16*)h->act, d);
     else
         attn_combine_kernel<float><<<grid2, thr, 0, h->stream>>>(h->y, 3 * d, (const float*)L.kc,
             (const float*)L.vc, (const float*)L.ks, (const float*)L.vs, H, dh, p.C, p.T, Q, g.q_max,
-            h->cfg.t_max, g.kv_splits, g.kv_chunk, p.kv_in_cache, h->kv_base, h->attn_part, (float*)h->act, d);
+            h->cfg.t_max, splits, chunk, p.kv_in_cache, h->kv_base, h->attn_part, (float*)h->act, d);
     h->launches++;
     prof_end(h, EVS_K_ATTN_COMBINE);
 }

@@ -141,8 +141,8 @@ def test_multi_candidate_fp32():
 
 def test_multi_candidate_sampling_bf16():
     wl = get_workload("tiny_d64_fp32").replace(
-        d=256, dtype="bf16", head_dim=64, batch=2, n_cand=4, gamma=6, mode="sampling",
-        layers=(LayerSpec("fir", 3), LayerSpec("iir", 16), LayerSpec("fir", 7), LayerSpec("attn", 4)))
+        d=256, dtype="bf16", head_dim=128, batch=2, n_cand=4, gamma=6, mode="sampling",
+        layers=(LayerSpec("fir", 3), LayerSpec("iir", 16), LayerSpec("fir", 7), LayerSpec("attn", 2)))
     pair = Pair(wl)
     pair.import_synthetic(300)
     _lockstep(pair, 4)
@@ -155,6 +155,25 @@ def test_bf16_small_stack_sampling():
     pair.prefill(wl.prefix_len)          # chunks of 128 and a ragged tail of 116
     pair.compare_state(tol=TOL["bf16"])
     _lockstep(pair, 5)
+
+
+def test_bf16_long_prefix_multi_tile_chunks():
+    """A prefix long enough that each attention CTA covers several 128-key tiles, with a
+    ragged last tile (40000 = 312 x 128 + 64)."""
+    wl = get_workload("d1024_l8_p8k_bf16").replace(d=256, head_dim=128, prefix_len=40000,
+        layers=(LayerSpec("fir", 3), LayerSpec("attn", 2)))
+    pair = Pair(wl)
+    pair.import_synthetic(wl.prefix_len)
+    _lockstep(pair, 3)
+
+
+def test_full_size_d1024_l8_p8k():
+    """The bench workload at full size (d=1024, 8 layers, 8192 cached tokens, gamma 6,
+    sampling), same kernels and launch shapes as the benchmark."""
+    wl = get_workload("d1024_l8_p8k_bf16")
+    pair = Pair(wl)
+    pair.import_synthetic(wl.prefix_len)
+    _lockstep(pair, 3)
 
 
 def test_host_errors():
