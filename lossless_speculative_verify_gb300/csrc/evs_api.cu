@@ -34,19 +34,30 @@ struct Profiler {
     }
 };
 
+// Inside stream capture a plain record only orders streams; an external record becomes an
+// event node of the graph, which is what timing needs.
+static void record(cudaEvent_t e, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(s, &cs);
+    if (cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+    else
+        cudaEventRecord(e, s);
+}
+
 void prof_begin(evs_handle* h, int kind) {
     (void)kind;
     if (!h->prof_on) return;
     Profiler* p = (Profiler*)h->prof;
     p->open = p->get();
-    cudaEventRecord(p->open, h->stream);
+    record(p->open, h->stream);
 }
 
 void prof_end(evs_handle* h, int kind) {
     if (!h->prof_on) return;
     Profiler* p = (Profiler*)h->prof;
     cudaEvent_t e = p->get();
-    cudaEventRecord(e, h->stream);
+    record(e, h->stream);
     p->recs.push_back({kind, p->open, e});
     p->open = nullptr;
 }
@@ -359,7 +370,11 @@ evs_status evs_profile_read(evs_handle* h, int32_t* launches, float* ms, int32_t
     if (cudaStreamSynchronize(h->stream) != cudaSuccess) return EVS_ERR_CUDA;
     for (auto& r : p->recs) {
         float t = 0.f;
-        if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) return EVS_ERR_CUDA;
+        if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) {
+            cudaGetLastError();  // not sticky: leave no error for later launches to report
+            p->recs.clear();
+            return EVS_ERR_CUDA;
+        }
         if (r.kind >= 0 && r.kind < n) { launches[r.kind] += 1; ms[r.kind] += t; }
         p->pool.push_back(r.a);
         p->pool.push_back(r.b);
