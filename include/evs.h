@@ -86,7 +86,7 @@ typedef struct {
     int32_t gamma;                        /* drafts per block (1..31)                   */
     int32_t batch;                        /* sequences B (1..64)                        */
     int32_t n_cand;                       /* candidate blocks C per sequence            */
-    int32_t t_max;                        /* KV capacity per sequence, tokens           */
+    int32_t t_max;                        /* KV capacity per sequence, tokens (<= 2^21) */
     int32_t prefill_chunk;                /* tokens per sequence per prefill pass       */
     int32_t dtype;                        /* EVS_DTYPE_*                                */
     int32_t mode;                         /* EVS_MODE_*                                 */

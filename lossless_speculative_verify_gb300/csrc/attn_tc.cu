@@ -40,7 +40,7 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int col_elem) {
     return (uint32_t)row * 128u + ((uint32_t)((col_elem >> 3) ^ (row & 7)) << 4) + (uint32_t)(col_elem & 7) * 2u;
 }
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(192, 2)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_slot[1];
@@ -300,8 +300,12 @@ AttnPlan attn_tc_plan(int Q, int B, int H, int t_max, int smem_max) {
     while (p.ncols < need) p.ncols <<= 1;
     // ring of 32 KiB stages in what is left of shared memory
     const int fixed = 1024 + 2 * p.n_q * 128 + p.tiles * 2 * p.n_q * 128 + 64 * 8;
-    p.stages = (smem_max - fixed) / AT_TILE_BYTES;
+    // keep two CTAs per SM when the chunk allows it, so one CTA's start-up and softmax
+    // overlap another's streaming
+    const int budget = fixed + 2 * AT_TILE_BYTES <= 110 * 1024 ? 110 * 1024 : smem_max;
+    p.stages = (budget - fixed) / AT_TILE_BYTES;
     if (p.stages > 4) p.stages = 4;
+    if (p.stages > 2 * p.tiles) p.stages = 2 * p.tiles;
     if (p.stages < 2) { p.n_q = 0; return p; }
     p.smem = fixed + p.stages * AT_TILE_BYTES;
     p.ok = 1;

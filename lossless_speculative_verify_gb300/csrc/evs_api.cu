@@ -95,7 +95,7 @@ bool valid_config(const evs_config* c) {
     if ((long long)c->batch * c->n_cand * (c->gamma + 1) > 512) return false;
     if (c->prefill_chunk < 1 || c->prefill_chunk > 128) return false;
     if ((long long)c->batch * c->prefill_chunk > 512) return false;
-    if (c->t_max < 1) return false;
+    if (c->t_max < 1 || c->t_max > (1 << 21)) return false;
     if (c->dtype != EVS_DTYPE_F32 && c->dtype != EVS_DTYPE_BF16) return false;
     if (c->mode != EVS_MODE_GREEDY && c->mode != EVS_MODE_SAMPLING) return false;
     if (!(c->temperature > 0.f) || !(c->near_tie_tau >= 0.f)) return false;

@@ -214,11 +214,14 @@ int gemm_tc_init() {
     return dyn;
 }
 
+// Split K only as far as each CTA still streams at least 8 k-blocks (128 KiB of weights),
+// and no further than filling the 152 SMs once: past that the partial-sum round trip and
+// the per-CTA start-up cost more than the extra parallelism returns.
 int tc_splits(int N, int K) {
     const int tiles = N / TC_BM, kblocks = K / TC_BK;
     int s = 152 / tiles;
+    if (s > kblocks / 8) s = kblocks / 8;
     if (s < 1) s = 1;
-    if (s > kblocks) s = kblocks;
     return s;
 }
 

@@ -304,61 +304,82 @@ __global__ void __launch_bounds__(256) attn_split_kernel(
 }
 
 // Merge the prefix partials with the in-block causal keys of the query's own candidate,
-// normalise, and store o in the projection dtype. One CTA per (sequence x head, query).
+// normalise, and store o in the projection dtype. One CTA per (sequence x head, query);
+// thread e owns output column e. Partials are fetched in parallel: first every split's
+// (m, l) by its own thread, then the in-block scores one warp per key, then o.
+constexpr int CMB_MAX_SPLITS = 1024;
+
 template <typename T>
-__global__ void attn_combine_kernel(const float* __restrict__ Y, int ldy, const T* __restrict__ kc,
-                                    const T* __restrict__ vc, const T* __restrict__ ks,
-                                    const T* __restrict__ vs, int H, int dh, int C, int Tb, int Q,
-                                    int q_max, int t_max, int splits, int chunk, int in_cache,
-                                    const int32_t* __restrict__ kv_base,
-                                    const float* __restrict__ part, T* __restrict__ out, int d) {
-    __shared__ float red[32];
+__global__ void __launch_bounds__(128) attn_combine_kernel(
+    const float* __restrict__ Y, int ldy, const T* __restrict__ kc, const T* __restrict__ vc,
+    const T* __restrict__ ks, const T* __restrict__ vs, int H, int dh, int C, int Tb, int Q, int q_max,
+    int t_max, int splits, int chunk, int in_cache, const int32_t* __restrict__ kv_base,
+    const float* __restrict__ part, T* __restrict__ out, int d) {
+    __shared__ float w_s[CMB_MAX_SPLITS];
+    __shared__ float l_s[CMB_MAX_SPLITS];
     __shared__ float sc_blk[128];
+    __shared__ float red[32];
     const int bh = blockIdx.x, qi = blockIdx.y, b = bh / H, hh = bh % H;
     const int c = qi / Tb, i = qi % Tb;
-    const int e = threadIdx.x;
-    const bool act = e < dh;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
     const int n = kv_base[b];  // rows n + j past t_max were never written (overflow flag set);
                                // their reads are clamped to stay in bounds
-    const int used = min((n + chunk - 1) / chunk, splits);  // splits that saw keys
+    const int used = min(min((n + chunk - 1) / chunk, splits), CMB_MAX_SPLITS);
+    const float* pbase = part + (((size_t)b * H + hh) * splits * q_max + qi) * (dh + 2);
+    const size_t pstride = (size_t)q_max * (dh + 2);
     float M = -INFINITY;
-    for (int s = 0; s < used; ++s) {
-        const float* p = part + ((((size_t)b * H + hh) * splits + s) * q_max + qi) * (dh + 2);
-        M = fmaxf(M, p[dh]);
+    for (int s = tid; s < used; s += blockDim.x) {
+        const float ms = pbase[s * pstride + dh];
+        w_s[s] = ms;
+        l_s[s] = pbase[s * pstride + dh + 1];
+        M = fmaxf(M, ms);
     }
-    // in-block scores q . k_j / sqrt(dh), j = 0..i
-    const float qv = act ? Y[((size_t)b * Q + qi) * ldy + hh * dh + e] : 0.f;
+    // in-block scores q . k_j / sqrt(dh), j = 0..i, one warp per key
     const float scale = rsqrtf((float)dh);
-    for (int j = 0; j <= i; ++j) {
-        float kval = 0.f;
-        if (act) {
-            kval = in_cache ? to_f32(kc[(((size_t)b * H + hh) * t_max + min(n + j, t_max - 1)) * dh + e])
-                            : to_f32(ks[((((size_t)(b * C + c)) * H + hh) * Tb + j) * dh + e]);
-        }
-        const float sj = block_sum(qv * kval, red) * scale;
-        if (e == 0) sc_blk[j] = sj;
-        M = fmaxf(M, sj);
+    const float* qrow = Y + ((size_t)b * Q + qi) * ldy + hh * dh;
+    for (int j = warp; j <= i; j += nw) {
+        const T* krow = in_cache ? kc + (((size_t)b * H + hh) * t_max + min(n + j, t_max - 1)) * dh
+                                 : ks + ((((size_t)(b * C + c)) * H + hh) * Tb + j) * dh;
+        float acc = 0.f;
+        for (int e = lane; e < dh; e += 32) acc = fmaf(qrow[e], to_f32(krow[e]), acc);
+        acc = warp_sum(acc) * scale;
+        if (lane == 0) sc_blk[j] = acc;
     }
     __syncthreads();
-    float L = 0.f, O = 0.f;
-    for (int s = 0; s < used; ++s) {
-        const float* p = part + ((((size_t)b * H + hh) * splits + s) * q_max + qi) * (dh + 2);
-        const float ms = p[dh];
-        if (ms == -INFINITY) continue;
-        const float w = __expf(ms - M);
-        L = fmaf(p[dh + 1], w, L);
-        if (act) O = fmaf(p[e], w, O);
+    for (int j = tid; j <= i; j += blockDim.x) M = fmaxf(M, sc_blk[j]);
+    M = block_max(M, red);
+    float L = 0.f;
+    for (int s = tid; s < used; s += blockDim.x) {
+        const float ms = w_s[s];
+        const float w = (ms == -INFINITY) ? 0.f : __expf(ms - M);
+        w_s[s] = w;
+        L = fmaf(l_s[s], w, L);
     }
-    for (int j = 0; j <= i; ++j) {
+    for (int j = tid; j <= i; j += blockDim.x) {
         const float w = __expf(sc_blk[j] - M);
+        sc_blk[j] = w;
         L += w;
-        if (act) {
+    }
+    L = block_sum(L, red);   // also orders the w_s / sc_blk writes before the reads below
+    for (int e = tid; e < dh; e += blockDim.x) {
+        float O = 0.f;
+        int s = 0;
+        for (; s + 4 <= used; s += 4) {
+            const float a0 = pbase[(s + 0) * pstride + e], a1 = pbase[(s + 1) * pstride + e];
+            const float a2 = pbase[(s + 2) * pstride + e], a3 = pbase[(s + 3) * pstride + e];
+            O = fmaf(a0, w_s[s], O);
+            O = fmaf(a1, w_s[s + 1], O);
+            O = fmaf(a2, w_s[s + 2], O);
+            O = fmaf(a3, w_s[s + 3], O);
+        }
+        for (; s < used; ++s) O = fmaf(pbase[s * pstride + e], w_s[s], O);
+        for (int j = 0; j <= i; ++j) {
             const float vval = in_cache ? to_f32(vc[(((size_t)b * H + hh) * t_max + min(n + j, t_max - 1)) * dh + e])
                                         : to_f32(vs[((((size_t)(b * C + c)) * H + hh) * Tb + j) * dh + e]);
-            O = fmaf(w, vval, O);
+            O = fmaf(sc_blk[j], vval, O);
         }
+        out[((size_t)b * Q + qi) * d + hh * dh + e] = from_f32<T>(O / L);
     }
-    if (act) out[((size_t)b * Q + qi) * d + hh * dh + e] = from_f32<T>(O / L);
 }
 
 // =========================================================================================
@@ -776,7 +797,7 @@ void launch_attention(evs_handle* h, int li, const Pass& p) {
     prof_end(h, EVS_K_ATTN);
     prof_begin(h, EVS_K_ATTN_COMBINE);
     dim3 grid2(p.B * H, Q);
-    const int thr = dh < 32 ? 32 : dh;
+    const int thr = 128;
     if (is_bf16(h))
         attn_combine_kernel<bf16><<<grid2, thr, 0, h->stream>>>(h->y, 3 * d, (const bf16*)L.kc,
             (const bf16*)L.vc, (const bf16*)L.ks, (const bf16*)L.vs, H, dh, p.C, p.T, Q, g.q_max, h->cfg.t_max,
