@@ -23,10 +23,17 @@ constexpr int TC_BM = 128;                    // output channels per tile (MMA M
 constexpr int TC_BK = 64;                     // K per stage: one 128-byte swizzled row of bf16
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2; // 16 KiB
 constexpr int TC_SMEM_BUDGET = 200 * 1024;
+#ifndef EVS_TC_KBS
+#define EVS_TC_KBS 4          // 64-wide k-blocks per pipeline stage (longer contiguous row reads)
+#endif
+#ifndef EVS_TC_ROTATE
+#define EVS_TC_ROTATE 0       // start each tile's k loop at a different offset
+#endif
 
 struct TcArgs {
     float* Y;
-    int ldy, M, N, kblocks, splits, n_pad, stages, accumulate, ncols;
+    int ldy, M, N, kblocks, splits, n_pad, stages, accumulate, ncols, kbs;
+    int cluster;      // 1: the splits of a tile form a cluster and reduce through DSMEM
     float* part;      // [splits][M][N] partial sums when splits > 1
     int* counters;    // [N / 128] arrival counters, zero between launches
     uint32_t* flags;
@@ -42,8 +49,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const int b_bytes = p.n_pad * 128;
     uint8_t* sA = smem;
-    uint8_t* sB = smem + (size_t)p.stages * TC_A_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + (size_t)p.stages * b_bytes);
+    uint8_t* sB = smem + (size_t)p.stages * p.kbs * TC_A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + (size_t)p.stages * p.kbs * b_bytes);
     uint64_t* empty = full + p.stages;
     uint64_t* done = empty + p.stages;
 
@@ -52,7 +59,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int n0 = tile * TC_BM;
     const int kb0 = (int)((long long)p.kblocks * split / p.splits);
     const int kb1 = (int)((long long)p.kblocks * (split + 1) / p.splits);
-    const int nk = kb1 - kb0;
+    const int nkb = kb1 - kb0;
+    const int nst = (nkb + p.kbs - 1) / p.kbs;              // pipeline steps of up to kbs k-blocks
+    const int rot = EVS_TC_ROTATE ? (tile * 5) % nst : 0;    // spread concurrent row offsets
+    const int a_stage = TC_A_BYTES * p.kbs, b_stage = b_bytes * p.kbs;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -78,15 +88,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // ---- producer: TMA ring ------------------------------------------------------
         const uint64_t pol_w = policy_evict_first();   // weights: read once
         const uint64_t pol_x = policy_evict_last();    // activations: read by every tile
-        for (int i = 0; i < nk; ++i) {
+        for (int i = 0; i < nst; ++i) {
             const int s = i % p.stages;
             const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
             if (i >= p.stages && !mbar_wait(&empty[s], ph ^ 1u)) { *abort_flag = 1; break; }
-            mbar_arrive_expect_tx(&full[s], (uint32_t)(TC_A_BYTES + b_bytes));
-            const int k = (kb0 + i) * TC_BK;
-            tma_load_2d(sA + (size_t)s * TC_A_BYTES, &tmA, k, n0, &full[s], pol_w);
-            for (int r = 0; r < p.n_pad; r += 256)
-                tma_load_2d(sB + (size_t)s * b_bytes + (size_t)r * 128, &tmB, k, r, &full[s], pol_x);
+            const int st = (i + rot) % nst;
+            const int k0 = kb0 + st * p.kbs;
+            const int cnt = min(p.kbs, kb1 - k0);
+            mbar_arrive_expect_tx(&full[s], (uint32_t)(cnt * (TC_A_BYTES + b_bytes)));
+            for (int j = 0; j < cnt; ++j) {
+                const int k = (k0 + j) * TC_BK;
+                tma_load_2d(sA + (size_t)s * a_stage + (size_t)j * TC_A_BYTES, &tmA, k, n0, &full[s], pol_w);
+                for (int r = 0; r < p.n_pad; r += 256)
+                    tma_load_2d(sB + (size_t)s * b_stage + (size_t)j * b_bytes + (size_t)r * 128, &tmB, k, r,
+                                &full[s], pol_x);
+            }
         }
     } else if (threadIdx.x == 32) {
         // ---- MMA issuer ------------------------------------------------------------------
@@ -94,19 +110,24 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int n_lo = p.n_pad - n_hi;
         const uint32_t id_lo = idesc_bf16_f32(TC_BM, n_lo);
         const uint32_t id_hi = idesc_bf16_f32(TC_BM, n_hi > 0 ? n_hi : 16);
-        for (int i = 0; i < nk; ++i) {
+        for (int i = 0; i < nst; ++i) {
             const int s = i % p.stages;
             const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
             if (!mbar_wait(&full[s], ph)) { *abort_flag = 1; break; }
             tc_fence_after();
-            const uint32_t a0 = smem_u32(sA + (size_t)s * TC_A_BYTES);
-            const uint32_t b0 = smem_u32(sB + (size_t)s * b_bytes);
+            const int st = (i + rot) % nst;
+            const int cnt = min(p.kbs, kb1 - (kb0 + st * p.kbs));
+            for (int j = 0; j < cnt; ++j) {
+                const uint32_t a0 = smem_u32(sA + (size_t)s * a_stage + (size_t)j * TC_A_BYTES);
+                const uint32_t b0 = smem_u32(sB + (size_t)s * b_stage + (size_t)j * b_bytes);
 #pragma unroll
-            for (int kk = 0; kk < TC_BK / 16; ++kk) {
-                const uint64_t ad = smem_desc_sw128(a0 + kk * 32);
-                const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                tc_mma_f16(tmem, ad, smem_desc_sw128(b0 + kk * 32), id_lo, acc);
-                if (n_hi > 0) tc_mma_f16(tmem + 256, ad, smem_desc_sw128(b0 + 256 * 128 + kk * 32), id_hi, acc);
+                for (int kk = 0; kk < TC_BK / 16; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(a0 + kk * 32);
+                    const uint32_t acc = (i > 0 || j > 0 || kk > 0) ? 1u : 0u;
+                    tc_mma_f16(tmem, ad, smem_desc_sw128(b0 + kk * 32), id_lo, acc);
+                    if (n_hi > 0)
+                        tc_mma_f16(tmem + 256, ad, smem_desc_sw128(b0 + 256 * 128 + kk * 32), id_hi, acc);
+                }
             }
             tc_commit(&empty[s]);
         }
@@ -135,6 +156,33 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
             }
         }
+    } else if (p.cluster) {
+        // split-K through distributed shared memory: every CTA of the cluster parks its
+        // partial tile [M][128] in its own (now idle) ring, then CTA r sums its share of the
+        // token columns across the cluster in a fixed order and writes them out
+        float* park = reinterpret_cast<float*>(smem);
+        for (int c0 = 0; c0 < p.M; c0 += 16) {
+            float v[16];
+            tmem_ld16(trow + (uint32_t)c0, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (c0 + j < p.M) park[(size_t)(c0 + j) * TC_BM + warp * 32 + lane] = v[j];
+        }
+        cluster_sync();
+        const int r = split;                      // rank in the cluster (cluster spans y)
+        const int m_lo = (int)((long long)p.M * r / p.splits), m_hi = (int)((long long)p.M * (r + 1) / p.splits);
+        const uint32_t base = smem_u32(park);
+        const int ch = threadIdx.x;               // channel within the tile
+        for (int m = m_lo; m < m_hi; ++m) {
+            const uint32_t off = base + (uint32_t)(m * TC_BM + ch) * 4u;
+            float acc = 0.f;
+            for (int sp = 0; sp < p.splits; ++sp) acc += ld_peer_f32(map_peer(off, (uint32_t)sp));
+            if (!bad && n0 + ch < p.N) {
+                float* dst = p.Y + (size_t)m * p.ldy + n0 + ch;
+                *dst = p.accumulate ? (*dst + acc) : acc;
+            }
+        }
+        cluster_sync();                           // peers finished reading this CTA's park
     } else {
         float* mine = p.part + (size_t)split * p.M * p.N;
         for (int c0 = 0; c0 < p.M; c0 += 16) {
@@ -153,11 +201,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (*last_flag) {
             __threadfence();
             if (col_ok) {
-                for (int m = 0; m < p.M; ++m) {
-                    float s = 0.f;
-                    for (int sp = 0; sp < p.splits; ++sp) s += __ldcg(p.part + ((size_t)sp * p.M + m) * p.N + n);
-                    float* dst = p.Y + (size_t)m * p.ldy + n;
-                    *dst = p.accumulate ? (*dst + s) : s;
+                // four rows at a time, every split's value requested before any is summed
+                for (int m0 = 0; m0 < p.M; m0 += 4) {
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int sp = 0; sp < p.splits; ++sp) {
+                        float v[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            v[u] = (m0 + u < p.M) ? __ldcg(p.part + ((size_t)sp * p.M + m0 + u) * p.N + n) : 0.f;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) acc[u] += v[u];
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        if (m0 + u >= p.M) break;
+                        float* dst = p.Y + (size_t)(m0 + u) * p.ldy + n;
+                        *dst = p.accumulate ? (*dst + acc[u]) : acc[u];
+                    }
                 }
             }
             if (threadIdx.x == 0) p.counters[tile] = 0;
@@ -225,6 +285,57 @@ int tc_splits(int N, int K) {
     return s;
 }
 
+// Launch shape of one projection: token padding, split-K, k-blocks per stage, ring depth,
+// TMEM columns and dynamic shared memory.
+struct TcShape {
+    int n_pad, tiles, kblocks, splits, kbs, stages, ncols, cluster, M_for_park;
+    size_t smem;
+};
+
+static TcShape tc_shape(int M, int N, int K) {
+    TcShape t{};
+    t.M_for_park = M;
+    // tokens padded to the MMA's N granularity; above 256 two accumulators of 256 columns
+    t.n_pad = M > 256 ? 512 : (M + 15) / 16 * 16;
+    t.tiles = N / TC_BM;
+    t.kblocks = K / TC_BK;
+    t.splits = tc_splits(N, K);
+    const int per = (t.kblocks + t.splits - 1) / t.splits;
+    t.kbs = EVS_TC_KBS;
+    const int kb_bytes = TC_A_BYTES + t.n_pad * 128;
+    while (t.kbs > 1 && (t.kbs > per || 2 * t.kbs * kb_bytes > TC_SMEM_BUDGET)) t.kbs >>= 1;
+    const int steps = (per + t.kbs - 1) / t.kbs;
+    t.stages = TC_SMEM_BUDGET / (t.kbs * kb_bytes);
+    if (t.stages > steps) t.stages = steps;
+    if (t.stages < 1) t.stages = 1;
+    t.ncols = 32;
+    while (t.ncols < t.n_pad) t.ncols <<= 1;
+    t.smem = (size_t)t.stages * t.kbs * kb_bytes + 1024 + (2 * t.stages + 1) * 8;
+    // cluster reduction when the splits fit a portable cluster and the partial tile fits the ring
+    t.cluster = t.splits > 1 && t.splits <= 8 &&
+                (size_t)t.M_for_park * TC_BM * 4 <= (size_t)t.stages * t.kbs * kb_bytes;
+    return t;
+}
+
+static bool launch_tc(const TcShape& t, const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a,
+                      cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(t.tiles, t.splits);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = t.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (t.cluster) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = (unsigned)t.splits;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, ta, tb, a) == cudaSuccess;
+}
+
 bool gemm_tc_supported(int M, int N, int K) {
     return M >= 1 && M <= 512 && N % TC_BM == 0 && K % TC_BK == 0 && N > 0 && K > 0;
 }
@@ -232,26 +343,14 @@ bool gemm_tc_supported(int M, int N, int K) {
 // Returns false (nothing launched) if a tensor map could not be built.
 bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, float* Y, int M, int N, int K,
                     int ldy, int accumulate) {
-    // tokens padded to the MMA's N granularity; above 256 two accumulators of 256 columns
-    const int n_pad = M > 256 ? 512 : (M + 15) / 16 * 16;
+    const TcShape t = tc_shape(M, N, K);
     CUtensorMap ta, tb;
     if (!make_map(&ta, W, (uint64_t)N, (uint64_t)K, TC_BM)) return false;
-    if (!make_map(&tb, X, (uint64_t)x_rows, (uint64_t)K, (uint32_t)(n_pad < 256 ? n_pad : 256))) return false;
-    const int tiles = N / TC_BM, kblocks = K / TC_BK;
-    const int splits = tc_splits(N, K);
-    const int per = (kblocks + splits - 1) / splits;
-    const int stage_bytes = TC_A_BYTES + n_pad * 128;
-    int stages = TC_SMEM_BUDGET / stage_bytes;
-    if (stages > per) stages = per;
-    if (stages < 1) stages = 1;
-    int ncols = 32;
-    while (ncols < n_pad) ncols <<= 1;
-    const size_t smem = (size_t)stages * stage_bytes + 1024 + (2 * stages + 1) * 8;
-    if ((int)smem > h->tc_smem_max) return false;
-    TcArgs a{Y, ldy, M, N, kblocks, splits, n_pad, stages, accumulate, ncols, h->gemm_part, h->gemm_counters,
-             h->flags};
-    gemm_tc_kernel<<<dim3(tiles, splits), 128, smem, h->stream>>>(ta, tb, a);
-    return true;
+    if (!make_map(&tb, X, (uint64_t)x_rows, (uint64_t)K, (uint32_t)(t.n_pad < 256 ? t.n_pad : 256))) return false;
+    if ((int)t.smem > h->tc_smem_max) return false;
+    TcArgs a{Y, ldy, M, N, t.kblocks, t.splits, t.n_pad, t.stages, accumulate, t.ncols, t.kbs, t.cluster,
+             h->gemm_part, h->gemm_counters, h->flags};
+    return launch_tc(t, ta, tb, a, h->stream);
 }
 
 }  // namespace evs
@@ -302,27 +401,18 @@ extern "C" evs_status evs_projection_noalloc(const void* X, int32_t x_rows, cons
         g_noalloc_ptr[dev] = p;
     }
     NoAllocScratch* sc = g_noalloc_ptr[dev];
-    const int splits = tc_splits(N, K);
-    if (splits > 1 && (size_t)splits * M * N > kNoAllocPartFloats) return EVS_ERR_CAPACITY;
-    const int n_pad = M > 256 ? 512 : (M + 15) / 16 * 16;
+    const TcShape t = tc_shape(M, N, K);
+    if (t.splits > 1 && (size_t)t.splits * M * N > kNoAllocPartFloats) return EVS_ERR_CAPACITY;
     CUtensorMap ta, tb;
     if (!make_map(&ta, W, (uint64_t)N, (uint64_t)K, TC_BM)) return EVS_ERR_CUDA;
-    if (!make_map(&tb, X, (uint64_t)x_rows, (uint64_t)K, (uint32_t)(n_pad < 256 ? n_pad : 256))) return EVS_ERR_CUDA;
-    const int tiles = N / TC_BM, kblocks = K / TC_BK;
-    const int per = (kblocks + splits - 1) / splits;
-    const int stage_bytes = TC_A_BYTES + n_pad * 128;
-    int stages = TC_SMEM_BUDGET / stage_bytes;
-    if (stages > per) stages = per;
-    if (stages < 1) stages = 1;
-    int ncols = 32;
-    while (ncols < n_pad) ncols <<= 1;
-    const size_t smem = (size_t)stages * stage_bytes + 1024 + (2 * stages + 1) * 8;
-    if ((int)smem > g_noalloc_smem[dev]) return EVS_ERR_INVALID_ARG;
+    if (!make_map(&tb, X, (uint64_t)x_rows, (uint64_t)K, (uint32_t)(t.n_pad < 256 ? t.n_pad : 256))) return EVS_ERR_CUDA;
+    if ((int)t.smem > g_noalloc_smem[dev]) return EVS_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
     // the array keeps the previous call's contents: the counters must start at zero
     if (cudaMemsetAsync(sc->counters, 0, sizeof(sc->counters), s) != cudaSuccess) return EVS_ERR_CUDA;
-    TcArgs a{Y, ldy, M, N, kblocks, splits, n_pad, stages, accumulate, ncols, sc->part, sc->counters, &sc->flags};
-    gemm_tc_kernel<<<dim3(tiles, splits), 128, smem, s>>>(ta, tb, a);
+    TcArgs a{Y, ldy, M, N, t.kblocks, t.splits, t.n_pad, t.stages, accumulate, t.ncols, t.kbs, t.cluster,
+             sc->part, sc->counters, &sc->flags};
+    if (!launch_tc(t, ta, tb, a, s)) return EVS_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? EVS_OK : EVS_ERR_CUDA;
 }
 
