@@ -48,6 +48,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     __shared__ float red[4][128];
     __shared__ float m_sh[128], l_sh[128];
 
+    pdl_trigger();
+    pdl_wait();
     const int split = blockIdx.x, bh = blockIdx.y;
     const int b = bh / a.H, head = bh % a.H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -333,8 +335,8 @@ bool launch_attn_tc(evs_handle* h, int li, const Pass& p, const AttnPlan& plan) 
         return false;
     AttnArgs a{h->y, 3 * h->cfg.d, H, p.C * p.T, plan.n_q, plan.tiles, plan.splits, h->g.q_max, plan.stages,
                plan.ncols, 1.0f / sqrtf((float)AT_DH), h->kv_base, h->attn_part, h->flags};
-    attn_tc_kernel<<<dim3(plan.splits, p.B * H), 192, plan.smem, h->stream>>>(tk, tv, a);
-    return true;
+    return launch_k(h, attn_tc_kernel, dim3(plan.splits, p.B * H), dim3(192), (size_t)plan.smem, tk, tv, a) ==
+           cudaSuccess;
 }
 
 }  // namespace evs

@@ -313,6 +313,7 @@ evs_status evs_create(const evs_config* cfg, const evs_weights* weights, void* w
     h->ws_bytes = ws_bytes;
     carve(*cfg, h->ws, h);
     h->tc_smem_max = 0;
+    h->pdl = 1;
     if (cfg->dtype == EVS_DTYPE_BF16) {
         h->tc_smem_max = evs::gemm_tc_init();
         const int attn_smem = evs::attn_tc_init();

@@ -50,4 +50,29 @@ __device__ __forceinline__ float block_max(float v, float* red) {
     return warp_max(t);
 }
 
+// ---- programmatic dependent launch -------------------------------------------------------
+// Every kernel of the library is launched so that it may start while its predecessor in the
+// stream drains. It lets its own dependents start (trigger) and, before touching any global
+// data a predecessor produced or may still read, waits for the predecessor grid to finish
+// (a no-op when launched without the attribute). Waiting in every kernel keeps the chain
+// transitive.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(evs_handle* h, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = h->stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = h->pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 }  // namespace evs

@@ -86,6 +86,7 @@ struct evs_handle {
     long long kv_hi;      // host upper bound of max_b kv_len
     int verified;         // a verify was enqueued since the last slice / prefill
     int launches;         // kernels enqueued by the last public call
+    int pdl;              // launch with programmatic dependent launch
     void* prof;           // evs::Profiler*, lazily created
     int prof_on;
 };

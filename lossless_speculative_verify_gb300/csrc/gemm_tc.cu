@@ -22,9 +22,21 @@ namespace evs {
 constexpr int TC_BM = 128;                    // output channels per tile (MMA M)
 constexpr int TC_BK = 64;                     // K per stage: one 128-byte swizzled row of bf16
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2; // 16 KiB
-constexpr int TC_SMEM_BUDGET = 200 * 1024;
+#ifndef EVS_TC_SMEM_KB
+#define EVS_TC_SMEM_KB 100     // shared-memory ring budget per CTA (two CTAs per SM)
+#endif
+#ifndef EVS_TC_CTA_TARGET
+#define EVS_TC_CTA_TARGET 304  // CTAs one projection aims to fill (two per SM)
+#endif
+#ifndef EVS_TC_MIN_KB
+#define EVS_TC_MIN_KB 8        // fewest 64-wide k-blocks a split may stream
+#endif
+constexpr int TC_SMEM_BUDGET = EVS_TC_SMEM_KB * 1024;
 #ifndef EVS_TC_KBS
 #define EVS_TC_KBS 4          // 64-wide k-blocks per pipeline stage (longer contiguous row reads)
+#endif
+#ifndef EVS_TC_PACKED
+#define EVS_TC_PACKED 0       // weights stored as contiguous [tile][k-block][128][64] blocks
 #endif
 #ifndef EVS_TC_ROTATE
 #define EVS_TC_ROTATE 0       // start each tile's k loop at a different offset
@@ -39,7 +51,7 @@ struct TcArgs {
     uint32_t* flags;
 };
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(128, 2)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcArgs p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_slot[1];
@@ -54,6 +66,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint64_t* empty = full + p.stages;
     uint64_t* done = empty + p.stages;
 
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x, split = blockIdx.y;
     const int n0 = tile * TC_BM;
@@ -88,21 +101,39 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // ---- producer: TMA ring ------------------------------------------------------
         const uint64_t pol_w = policy_evict_first();   // weights: read once
         const uint64_t pol_x = policy_evict_last();    // activations: read by every tile
-        for (int i = 0; i < nst; ++i) {
+        auto load = [&](int i, bool a, bool b) {
             const int s = i % p.stages;
-            const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
-            if (i >= p.stages && !mbar_wait(&empty[s], ph ^ 1u)) { *abort_flag = 1; break; }
             const int st = (i + rot) % nst;
             const int k0 = kb0 + st * p.kbs;
             const int cnt = min(p.kbs, kb1 - k0);
-            mbar_arrive_expect_tx(&full[s], (uint32_t)(cnt * (TC_A_BYTES + b_bytes)));
+            if (a) mbar_arrive_expect_tx(&full[s], (uint32_t)(cnt * (TC_A_BYTES + b_bytes)));
             for (int j = 0; j < cnt; ++j) {
                 const int k = (k0 + j) * TC_BK;
-                tma_load_2d(sA + (size_t)s * a_stage + (size_t)j * TC_A_BYTES, &tmA, k, n0, &full[s], pol_w);
-                for (int r = 0; r < p.n_pad; r += 256)
-                    tma_load_2d(sB + (size_t)s * b_stage + (size_t)j * b_bytes + (size_t)r * 128, &tmB, k, r,
-                                &full[s], pol_x);
+                if (a) {
+#if EVS_TC_PACKED
+                    tma_load_2d(sA + (size_t)s * a_stage + (size_t)j * TC_A_BYTES, &tmA, 0,
+                                (tile * p.kblocks + k0 + j) * TC_BM, &full[s], pol_w);
+#else
+                    tma_load_2d(sA + (size_t)s * a_stage + (size_t)j * TC_A_BYTES, &tmA, k, n0, &full[s], pol_w);
+#endif
+                }
+                if (b)
+                    for (int r = 0; r < p.n_pad; r += 256)
+                        tma_load_2d(sB + (size_t)s * b_stage + (size_t)j * b_bytes + (size_t)r * 128, &tmB, k, r,
+                                    &full[s], pol_x);
             }
+        };
+        // weights do not depend on the previous kernel: fill the ring with them before
+        // waiting for it, then add the activations
+        const int pre = min(p.stages, nst);
+        for (int i = 0; i < pre; ++i) load(i, true, false);
+        pdl_wait();
+        for (int i = 0; i < pre; ++i) load(i, false, true);
+        for (int i = pre; i < nst; ++i) {
+            const int s = i % p.stages;
+            const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
+            if (!mbar_wait(&empty[s], ph ^ 1u)) { *abort_flag = 1; break; }
+            load(i, true, true);
         }
     } else if (threadIdx.x == 32) {
         // ---- MMA issuer ------------------------------------------------------------------
@@ -135,6 +166,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
 
     // ---- epilogue: lane = output channel, columns = tokens ---------------------------------
+    pdl_wait();
     __syncwarp();
     const bool ok = mbar_wait(done, 0);
     tc_fence_after();
@@ -279,8 +311,8 @@ int gemm_tc_init() {
 // the per-CTA start-up cost more than the extra parallelism returns.
 int tc_splits(int N, int K) {
     const int tiles = N / TC_BM, kblocks = K / TC_BK;
-    int s = 152 / tiles;
-    if (s > kblocks / 8) s = kblocks / 8;
+    int s = EVS_TC_CTA_TARGET / tiles;
+    if (s > kblocks / EVS_TC_MIN_KB) s = kblocks / EVS_TC_MIN_KB;
     if (s < 1) s = 1;
     return s;
 }
@@ -318,21 +350,28 @@ static TcShape tc_shape(int M, int N, int K) {
 }
 
 static bool launch_tc(const TcShape& t, const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& a,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(t.tiles, t.splits);
     cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = t.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    int n = 0;
     if (t.cluster) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 1;
-        attr[0].val.clusterDim.y = (unsigned)t.splits;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 1;
+        attr[n].val.clusterDim.y = (unsigned)t.splits;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
     }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, ta, tb, a) == cudaSuccess;
 }
 
@@ -345,12 +384,16 @@ bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, flo
                     int ldy, int accumulate) {
     const TcShape t = tc_shape(M, N, K);
     CUtensorMap ta, tb;
+#if EVS_TC_PACKED
+    if (!make_map(&ta, W, (uint64_t)N * K / TC_BK, (uint64_t)TC_BK, TC_BM)) return false;
+#else
     if (!make_map(&ta, W, (uint64_t)N, (uint64_t)K, TC_BM)) return false;
+#endif
     if (!make_map(&tb, X, (uint64_t)x_rows, (uint64_t)K, (uint32_t)(t.n_pad < 256 ? t.n_pad : 256))) return false;
     if ((int)t.smem > h->tc_smem_max) return false;
     TcArgs a{Y, ldy, M, N, t.kblocks, t.splits, t.n_pad, t.stages, accumulate, t.ncols, t.kbs, t.cluster,
              h->gemm_part, h->gemm_counters, h->flags};
-    return launch_tc(t, ta, tb, a, h->stream);
+    return launch_tc(t, ta, tb, a, h->stream, h->pdl != 0);
 }
 
 }  // namespace evs
@@ -412,7 +455,7 @@ extern "C" evs_status evs_projection_noalloc(const void* X, int32_t x_rows, cons
     if (cudaMemsetAsync(sc->counters, 0, sizeof(sc->counters), s) != cudaSuccess) return EVS_ERR_CUDA;
     TcArgs a{Y, ldy, M, N, t.kblocks, t.splits, t.n_pad, t.stages, accumulate, t.ncols, t.kbs, t.cluster,
              sc->part, sc->counters, &sc->flags};
-    if (!launch_tc(t, ta, tb, a, s)) return EVS_ERR_CUDA;
+    if (!launch_tc(t, ta, tb, a, s, false)) return EVS_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? EVS_OK : EVS_ERR_CUDA;
 }
 

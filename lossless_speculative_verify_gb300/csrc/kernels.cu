@@ -18,6 +18,8 @@ __global__ void embed_kernel(const T* __restrict__ E, const int32_t* __restrict_
                              float* __restrict__ h, int d, int C, int Tb, int vocab, int B,
                              const int32_t* __restrict__ kv_len, int32_t* __restrict__ kv_base,
                              uint32_t* __restrict__ flags) {
+    pdl_trigger();
+    pdl_wait();
     const int m = blockIdx.x;
     const int bc = m / Tb, i = m % Tb, b = bc / C;
     int tok = (i == 0 && anchor != nullptr) ? anchor[b] : tokens[(size_t)bc * tok_stride_bc + i];
@@ -37,6 +39,8 @@ __global__ void embed_kernel(const T* __restrict__ E, const int32_t* __restrict_
 // =========================================================================================
 template <typename T>
 __global__ void rmsnorm_kernel(const float* __restrict__ h, T* __restrict__ out, int d) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[32];
     const int m = blockIdx.x;
     const float* row = h + (size_t)m * d;
@@ -57,6 +61,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(const T* __restrict__ A, const T* __restrict__ W,
                                                         float* __restrict__ Y, int M, int N, int K,
                                                         int ldy, int accumulate) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float As[GS_BM][GS_BK + 1];
     __shared__ float Ws[GS_BN][GS_BK + 1];
     const int tid = threadIdx.x;
@@ -102,6 +108,8 @@ template <typename T>
 __global__ void fir_kernel(const float* __restrict__ Y, int ldy, T* __restrict__ out, int d,
                            int C, int Tb, int commit, const float* __restrict__ taps, int L,
                            float* __restrict__ tail, float* __restrict__ stage) {
+    pdl_trigger();
+    pdl_wait();
     const int ch = blockIdx.x * blockDim.x + threadIdx.x;
     const int bc = blockIdx.y, b = bc / C;
     if (ch >= d) return;
@@ -145,6 +153,8 @@ __global__ void iir_kernel(const float* __restrict__ Y, int ldy, T* __restrict__
                            int N, int C, int Tb, int commit, const float2* __restrict__ lam,
                            const float2* __restrict__ bb, const float2* __restrict__ cc,
                            float2* __restrict__ state, float2* __restrict__ ret) {
+    pdl_trigger();
+    pdl_wait();
     const int g = blockIdx.x * blockDim.x + threadIdx.x;
     const int bc = blockIdx.y, b = bc / C;
     if (g >= d * N) return;  // d*N is a multiple of 32: whole warps leave together
@@ -174,6 +184,8 @@ __global__ void kv_write_kernel(const float* __restrict__ Y, int ldy, int d, int
                                 int Tb, int in_cache, int t_max, const int32_t* __restrict__ kv_base,
                                 T* __restrict__ kc, T* __restrict__ vc, T* __restrict__ ks,
                                 T* __restrict__ vs, uint32_t* __restrict__ flags) {
+    pdl_trigger();
+    pdl_wait();
     const int m = blockIdx.y;
     const int col = blockIdx.x * blockDim.x + threadIdx.x;
     if (col >= d) return;
@@ -208,6 +220,8 @@ __global__ void __launch_bounds__(256) attn_split_kernel(
     const float* __restrict__ Y, int ldy, const T* __restrict__ kc, const T* __restrict__ vc, int H,
     int dh, int Q, int q_max, int t_max, int chunk, int splits, const int32_t* __restrict__ kv_base,
     float* __restrict__ part) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float qs[AQ][128];
     __shared__ float kvs[AK][129];
     __shared__ float ps[AQ][AK];
@@ -315,6 +329,8 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(
     const T* __restrict__ ks, const T* __restrict__ vs, int H, int dh, int C, int Tb, int Q, int q_max,
     int t_max, int splits, int chunk, int in_cache, const int32_t* __restrict__ kv_base,
     const float* __restrict__ part, T* __restrict__ out, int d) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float w_s[CMB_MAX_SPLITS];
     __shared__ float l_s[CMB_MAX_SPLITS];
     __shared__ float sc_blk[128];
@@ -505,6 +521,8 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(
     const float* __restrict__ unif, int32_t* __restrict__ cand_k, int32_t* __restrict__ cand_corr,
     uint32_t* __restrict__ cand_tie, int32_t* __restrict__ out_k, int32_t* __restrict__ out_corr,
     int32_t* __restrict__ out_cand, uint32_t* __restrict__ out_tie, uint32_t* __restrict__ flags) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float redf[32];
     __shared__ int redi[32];
     __shared__ float redv[32];
@@ -618,6 +636,8 @@ __global__ void slice_kernel(const LayerDesc* __restrict__ layers, int n_layers,
                              const int32_t* __restrict__ kin, const int32_t* __restrict__ cin,
                              const int32_t* __restrict__ kv_base, int32_t* __restrict__ kv_len,
                              uint32_t* __restrict__ flags) {
+    pdl_trigger();
+    pdl_wait();
     const int b = blockIdx.x;
     const int k = kin[b];
     const int c = cin ? cin[b] : 0;
@@ -664,6 +684,8 @@ __global__ void slice_kernel(const LayerDesc* __restrict__ layers, int n_layers,
 
 __global__ void advance_kernel(const int32_t* __restrict__ kv_base, int32_t* __restrict__ kv_len,
                                int B, int T, int t_max, uint32_t* __restrict__ flags) {
+    pdl_trigger();
+    pdl_wait();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
     int nl = kv_base[b] + T;
@@ -682,10 +704,10 @@ void launch_embed(evs_handle* h, const int32_t* tokens, int tok_stride_bc, const
     prof_begin(h, EVS_K_EMBED);
     const int d = h->cfg.d;
     if (is_bf16(h))
-        embed_kernel<bf16><<<p.M, 256, 0, h->stream>>>((const bf16*)h->w.embed, tokens, tok_stride_bc,
+        launch_k(h, embed_kernel<bf16>, dim3(p.M), dim3(256), 0, (const bf16*)h->w.embed, tokens, tok_stride_bc,
             anchor, h->h, d, p.C, p.T, h->cfg.vocab, p.B, h->kv_len, h->kv_base, h->flags);
     else
-        embed_kernel<float><<<p.M, 256, 0, h->stream>>>((const float*)h->w.embed, tokens, tok_stride_bc,
+        launch_k(h, embed_kernel<float>, dim3(p.M), dim3(256), 0, (const float*)h->w.embed, tokens, tok_stride_bc,
             anchor, h->h, d, p.C, p.T, h->cfg.vocab, p.B, h->kv_len, h->kv_base, h->flags);
     h->launches++;
     prof_end(h, EVS_K_EMBED);
@@ -694,8 +716,8 @@ void launch_embed(evs_handle* h, const int32_t* tokens, int tok_stride_bc, const
 void launch_rmsnorm(evs_handle* h, const Pass& p) {
     prof_begin(h, EVS_K_NORM);
     const int d = h->cfg.d;
-    if (is_bf16(h)) rmsnorm_kernel<bf16><<<p.M, 256, 0, h->stream>>>(h->h, (bf16*)h->act, d);
-    else rmsnorm_kernel<float><<<p.M, 256, 0, h->stream>>>(h->h, (float*)h->act, d);
+    if (is_bf16(h)) launch_k(h, rmsnorm_kernel<bf16>, dim3(p.M), dim3(256), 0, h->h, (bf16*)h->act, d);
+    else launch_k(h, rmsnorm_kernel<float>, dim3(p.M), dim3(256), 0, h->h, (float*)h->act, d);
     h->launches++;
     prof_end(h, EVS_K_NORM);
 }
@@ -711,10 +733,10 @@ void launch_gemm(evs_handle* h, const void* A, const void* W, float* Y, int M, i
     }
     dim3 grid((N + GS_BN - 1) / GS_BN, (M + GS_BM - 1) / GS_BM);
     if (is_bf16(h))
-        gemm_simt_kernel<bf16><<<grid, 256, 0, h->stream>>>((const bf16*)A, (const bf16*)W, Y, M, N, K, ldy,
+        launch_k(h, gemm_simt_kernel<bf16>, dim3(grid), dim3(256), 0, (const bf16*)A, (const bf16*)W, Y, M, N, K, ldy,
                                                              accumulate);
     else
-        gemm_simt_kernel<float><<<grid, 256, 0, h->stream>>>((const float*)A, (const float*)W, Y, M, N, K,
+        launch_k(h, gemm_simt_kernel<float>, dim3(grid), dim3(256), 0, (const float*)A, (const float*)W, Y, M, N, K,
                                                               ldy, accumulate);
     h->launches++;
     prof_end(h, EVS_K_GEMM);
@@ -727,10 +749,10 @@ void launch_fir(evs_handle* h, int li, const Pass& p) {
     dim3 grid((d + 127) / 128, p.B * p.C);
     const float* taps = h->w.layer[li].fir_taps;
     if (is_bf16(h))
-        fir_kernel<bf16><<<grid, 128, 0, h->stream>>>(h->y, 3 * d, (bf16*)h->act, d, p.C, p.T, p.commit, taps,
+        launch_k(h, fir_kernel<bf16>, dim3(grid), dim3(128), 0, h->y, 3 * d, (bf16*)h->act, d, p.C, p.T, p.commit, taps,
                                                        L.param, L.tail, L.stage);
     else
-        fir_kernel<float><<<grid, 128, 0, h->stream>>>(h->y, 3 * d, (float*)h->act, d, p.C, p.T, p.commit,
+        launch_k(h, fir_kernel<float>, dim3(grid), dim3(128), 0, h->y, 3 * d, (float*)h->act, d, p.C, p.T, p.commit,
                                                         taps, L.param, L.tail, L.stage);
     h->launches++;
     prof_end(h, EVS_K_FIR);
@@ -746,10 +768,10 @@ void launch_iir(evs_handle* h, int li, const Pass& p) {
     const float2* bb = (const float2*)h->w.layer[li].iir_b;
     const float2* cc = (const float2*)h->w.layer[li].iir_c;
     if (is_bf16(h))
-        iir_kernel<bf16><<<grid, 256, 0, h->stream>>>(h->y, 3 * d, (bf16*)h->act, d, N, p.C, p.T, p.commit,
+        launch_k(h, iir_kernel<bf16>, dim3(grid), dim3(256), 0, h->y, 3 * d, (bf16*)h->act, d, N, p.C, p.T, p.commit,
                                                        lam, bb, cc, L.state, L.ret);
     else
-        iir_kernel<float><<<grid, 256, 0, h->stream>>>(h->y, 3 * d, (float*)h->act, d, N, p.C, p.T, p.commit,
+        launch_k(h, iir_kernel<float>, dim3(grid), dim3(256), 0, h->y, 3 * d, (float*)h->act, d, N, p.C, p.T, p.commit,
                                                         lam, bb, cc, L.state, L.ret);
     h->launches++;
     prof_end(h, EVS_K_IIR);
@@ -762,10 +784,10 @@ void launch_kv_write(evs_handle* h, int li, const Pass& p) {
     const int H = L.param, dh = h->cfg.head_dim;
     dim3 grid((d + 255) / 256, p.M);
     if (is_bf16(h))
-        kv_write_kernel<bf16><<<grid, 256, 0, h->stream>>>(h->y, 3 * d, d, H, dh, p.C, p.T, p.kv_in_cache,
+        launch_k(h, kv_write_kernel<bf16>, dim3(grid), dim3(256), 0, h->y, 3 * d, d, H, dh, p.C, p.T, p.kv_in_cache,
             h->cfg.t_max, h->kv_base, (bf16*)L.kc, (bf16*)L.vc, (bf16*)L.ks, (bf16*)L.vs, h->flags);
     else
-        kv_write_kernel<float><<<grid, 256, 0, h->stream>>>(h->y, 3 * d, d, H, dh, p.C, p.T, p.kv_in_cache,
+        launch_k(h, kv_write_kernel<float>, dim3(grid), dim3(256), 0, h->y, 3 * d, d, H, dh, p.C, p.T, p.kv_in_cache,
             h->cfg.t_max, h->kv_base, (float*)L.kc, (float*)L.vc, (float*)L.ks, (float*)L.vs, h->flags);
     h->launches++;
     prof_end(h, EVS_K_KV_WRITE);
@@ -786,10 +808,10 @@ void launch_attention(evs_handle* h, int li, const Pass& p) {
     } else {
     dim3 grid(g.kv_splits, p.B * H, (Q + AQ - 1) / AQ);
     if (is_bf16(h))
-        attn_split_kernel<bf16><<<grid, 256, 0, h->stream>>>(h->y, 3 * d, (const bf16*)L.kc, (const bf16*)L.vc,
+        launch_k(h, attn_split_kernel<bf16>, dim3(grid), dim3(256), 0, h->y, 3 * d, (const bf16*)L.kc, (const bf16*)L.vc,
             H, dh, Q, g.q_max, h->cfg.t_max, g.kv_chunk, g.kv_splits, h->kv_base, h->attn_part);
     else
-        attn_split_kernel<float><<<grid, 256, 0, h->stream>>>(h->y, 3 * d, (const float*)L.kc,
+        launch_k(h, attn_split_kernel<float>, dim3(grid), dim3(256), 0, h->y, 3 * d, (const float*)L.kc,
             (const float*)L.vc, H, dh, Q, g.q_max, h->cfg.t_max, g.kv_chunk, g.kv_splits, h->kv_base,
             h->attn_part);
     }
@@ -799,11 +821,11 @@ void launch_attention(evs_handle* h, int li, const Pass& p) {
     dim3 grid2(p.B * H, Q);
     const int thr = 128;
     if (is_bf16(h))
-        attn_combine_kernel<bf16><<<grid2, thr, 0, h->stream>>>(h->y, 3 * d, (const bf16*)L.kc,
+        launch_k(h, attn_combine_kernel<bf16>, dim3(grid2), dim3(thr), 0, h->y, 3 * d, (const bf16*)L.kc,
             (const bf16*)L.vc, (const bf16*)L.ks, (const bf16*)L.vs, H, dh, p.C, p.T, Q, g.q_max, h->cfg.t_max,
             splits, chunk, p.kv_in_cache, h->kv_base, h->attn_part, (bf16*)h->act, d);
     else
-        attn_combine_kernel<float><<<grid2, thr, 0, h->stream>>>(h->y, 3 * d, (const float*)L.kc,
+        launch_k(h, attn_combine_kernel<float>, dim3(grid2), dim3(thr), 0, h->y, 3 * d, (const float*)L.kc,
             (const float*)L.vc, (const float*)L.ks, (const float*)L.vs, H, dh, p.C, p.T, Q, g.q_max,
             h->cfg.t_max, splits, chunk, p.kv_in_cache, h->kv_base, h->attn_part, (float*)h->act, d);
     h->launches++;
@@ -818,7 +840,7 @@ void launch_accept(evs_handle* h, const int32_t* tokens, const float* q, const f
     const float inv_t = 1.0f / c.temperature;
     const int Tb = c.gamma + 1;
 #define EVS_ACC(VPT)                                                                              \
-    accept_kernel<VPT><<<c.batch, ACC_THREADS, 0, h->stream>>>(h->logits, V, c.n_cand, Tb, c.gamma,   \
+    launch_k(h, accept_kernel<VPT>, dim3(c.batch), dim3(ACC_THREADS), 0, h->logits, V, c.n_cand, Tb, c.gamma,   \
         c.mode, inv_t, c.near_tie_tau, tokens, q, u, h->cand_k, h->cand_corr, h->cand_tie, acc, corr, \
         cand, tie, h->flags)
     switch (V / ACC_THREADS) {
@@ -838,10 +860,10 @@ void launch_slice(evs_handle* h, const int32_t* k, const int32_t* cand) {
     const evs_config& c = h->cfg;
     dim3 grid(c.batch, 16);
     if (is_bf16(h))
-        slice_kernel<bf16><<<grid, 256, 0, h->stream>>>(h->layer_dev, c.n_layers, c.d, c.head_dim, c.n_cand,
+        launch_k(h, slice_kernel<bf16>, dim3(grid), dim3(256), 0, h->layer_dev, c.n_layers, c.d, c.head_dim, c.n_cand,
             c.gamma + 1, c.gamma, c.t_max, k, cand, h->kv_base, h->kv_len, h->flags);
     else
-        slice_kernel<float><<<grid, 256, 0, h->stream>>>(h->layer_dev, c.n_layers, c.d, c.head_dim, c.n_cand,
+        launch_k(h, slice_kernel<float>, dim3(grid), dim3(256), 0, h->layer_dev, c.n_layers, c.d, c.head_dim, c.n_cand,
             c.gamma + 1, c.gamma, c.t_max, k, cand, h->kv_base, h->kv_len, h->flags);
     h->launches++;
     prof_end(h, EVS_K_SLICE);
@@ -849,7 +871,7 @@ void launch_slice(evs_handle* h, const int32_t* k, const int32_t* cand) {
 
 void launch_advance(evs_handle* h, int T) {
     prof_begin(h, EVS_K_ADVANCE);
-    advance_kernel<<<1, 256, 0, h->stream>>>(h->kv_base, h->kv_len, h->cfg.batch, T, h->cfg.t_max, h->flags);
+    launch_k(h, advance_kernel, dim3(1), dim3(256), 0, h->kv_base, h->kv_len, h->cfg.batch, T, h->cfg.t_max, h->flags);
     h->launches++;
     prof_end(h, EVS_K_ADVANCE);
 }
