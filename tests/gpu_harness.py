@@ -34,6 +34,13 @@ def make_verifier(wl, weights, t_max, near_tie_tau=None):
     return Verifier(cfg, dw)
 
 
+def _select(st, seqs):
+    out = {"kv_len": st["kv_len"][seqs], "layers": []}
+    for L in st["layers"]:
+        out["layers"].append({k: (v[seqs] if k != "kind" else v) for k, v in L.items()})
+    return out
+
+
 class RoundOut:
     """own / kern: oracle decisions (k_c, corr_c, tie_c, k, corr, cand, tie) from its own
     fp64 logits and from the library's fp32 logits; gk, gc, gcand: the library's."""
@@ -66,9 +73,9 @@ class Pair:
             oracle.prefill(self.tgt, self.states[b], toks[b])
         self.ver.prefill(torch.as_tensor(toks, dtype=torch.int32).cuda().contiguous())
 
-    def import_synthetic(self, P):
+    def import_synthetic(self, P, kv_dtype=np.float64):
         st = gen_state(self.wl, P)
-        self.states = [self.tgt.state_from_arrays(st, b) for b in range(self.wl.batch)]
+        self.states = [self.tgt.state_from_arrays(st, b, kv_dtype=kv_dtype) for b in range(self.wl.batch)]
         self.ver.import_state(st)
 
     def oracle_state_arrays(self):
@@ -94,18 +101,23 @@ class Pair:
                                       "s": np.stack([s.layers[li]["s"] for s in self.states])})
         return out
 
-    def compare_state(self, tol=None):
+    def compare_state(self, tol=None, seqs=None, kv_from=0):
+        """Exported library state against the oracle's. seqs limits the sequences compared;
+        kv_from skips cache rows below it (rows the round did not touch)."""
         tol = TOL[self.wl.dtype] if tol is None else tol
         g = self.ver.export_state()
         o = self.oracle_state_arrays()
+        if seqs is not None:
+            g = _select(g, seqs)
+            o = _select(o, seqs)
         np.testing.assert_array_equal(g["kv_len"], o["kv_len"])
         worst = 0.0
         for li, (a, b) in enumerate(zip(g["layers"], o["layers"])):
             if a["kind"] == "attn":
-                for bb in range(self.wl.batch):
+                for bb in range(len(o["kv_len"])):
                     n = int(o["kv_len"][bb])
                     for key in ("k", "v"):
-                        e = rel_l2(a[key][bb, :, :n], b[key][bb, :, :n])
+                        e = rel_l2(a[key][bb, :, kv_from:n], b[key][bb, :, kv_from:n])
                         assert e <= tol, f"layer {li} {key} seq {bb}: rel err {e:.3e}"
                         worst = max(worst, e)
             elif a["kind"] == "fir":
@@ -118,12 +130,42 @@ class Pair:
                 worst = max(worst, e)
         return worst
 
+    def compare_state_light(self, seqs, rows_from, tol=None):
+        """Sliced state of the given sequences through read-only views of the library's
+        buffers (no full export): kv_len, FIR tails, IIR states and the cache rows from
+        rows_from to kv_len (the rows a round writes)."""
+        wl = self.wl
+        tol = TOL[wl.dtype] if tol is None else tol
+        B, d, dh = wl.batch, wl.d, wl.head_dim
+        tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+        kvl = self.ver.buffer(7, -1, torch.int32, (B,)).cpu().numpy()
+        for b in seqs:
+            st = self.states[b]
+            assert kvl[b] == st.kv_len, (b, kvl[b], st.kv_len)
+            for li, spec in enumerate(wl.layers):
+                L = st.layers[li]
+                if spec.kind == "fir":
+                    t = self.ver.buffer(8, li, torch.float32, (B, spec.param - 1, d))[b].cpu().numpy()
+                    e = rel_l2(t, L["tail"])
+                elif spec.kind == "iir":
+                    t = self.ver.buffer(9, li, torch.float32, (B, d, spec.param, 2))[b].cpu().numpy()
+                    e = rel_l2(t, np.stack([L["s"].real, L["s"].imag], axis=-1))
+                else:
+                    H = spec.param
+                    n = st.kv_len
+                    for which, arr in ((3, L["kv"].k), (4, L["kv"].v)):
+                        c = self.ver.buffer(which, li, tdt, (B, H, self.t_max, dh))[b, :, rows_from:n]
+                        e = rel_l2(c.float().cpu().numpy(), arr[:, rows_from:n])
+                        assert e <= tol, f"layer {li} cache rows: rel err {e:.3e}"
+                    continue
+                assert e <= tol, f"layer {li} {spec.kind} state: rel err {e:.3e}"
+
     # ---- one round -------------------------------------------------------------------------
     def round_inputs(self, r, anchor=None):
         rnd = gen_round(self.wl, r, anchor=anchor)
         return rnd
 
-    def run_round(self, rnd, check_block=True, tol=None):
+    def run_round(self, rnd, check_block=True, tol=None, seqs=None):
         """Verify + slice on both sides from the current (identical) state.
 
         Decisions are checked in two ways: (1) the oracle's acceptance applied to the
@@ -139,57 +181,61 @@ class Pair:
         sampling = wl.mode == "sampling"
         q = dev(rnd["q"], torch.float32) if sampling else None
         u = dev(rnd["u"], torch.float32) if sampling else None
-        bp = oracle.block_pass(self.tgt, self.states, rnd["tokens"])
-        own = oracle.accept_block(bp["logits"], rnd["tokens"], rnd["q"], rnd["u"], wl.mode,
-                                  wl.temperature, TAU[wl.dtype])
+        sq = list(range(wl.batch)) if seqs is None else list(seqs)
+        sub = lambda a: None if a is None else np.asarray(a)[sq]
+        states = [self.states[b] for b in sq]
+        bp = oracle.block_pass(self.tgt, states, sub(rnd["tokens"]))
+        own = oracle.accept_block(bp["logits"], sub(rnd["tokens"]), sub(rnd["q"]), sub(rnd["u"]),
+                                  wl.mode, wl.temperature, TAU[wl.dtype])
         k, corr, cand, tie = self.ver.verify(toks, q, u)
         torch.cuda.synchronize()
         if check_block:
-            self.check_block(bp, tol)
+            self.check_block(bp, tol, sq)
         B, C, T, V = wl.batch, wl.n_cand, wl.block, wl.vocab
-        glog = self.ver.buffer(0, -1, torch.float32, (B, C, T, V)).cpu().numpy()
-        kern = oracle.accept_block(glog, rnd["tokens"], rnd["q"], rnd["u"], wl.mode,
+        glog = self.ver.buffer(0, -1, torch.float32, (B, C, T, V)).cpu().numpy()[sq]
+        kern = oracle.accept_block(glog, sub(rnd["tokens"]), sub(rnd["q"]), sub(rnd["u"]), wl.mode,
                                    wl.temperature, TAU["f32"])
-        gk, gc, gcand = k.cpu().numpy(), corr.cpu().numpy(), cand.cpu().numpy()
+        gk, gc, gcand = k.cpu().numpy()[sq], corr.cpu().numpy()[sq], cand.cpu().numpy()[sq]
         gcand = gcand if C > 1 else np.zeros_like(gk)
-        for b in range(B):
-            if kern[6][b]:
+        for i in range(len(sq)):
+            if kern[6][i]:
                 continue
-            assert gk[b] == kern[3][b] and gc[b] == kern[4][b] and gcand[b] == kern[5][b], \
-                (b, gk, gc, gcand, kern[3:6])
-        oracle.commit(self.states, bp, gk, gcand)
+            assert gk[i] == kern[3][i] and gc[i] == kern[4][i] and gcand[i] == kern[5][i], \
+                (sq[i], gk, gc, gcand, kern[3:6])
+        oracle.commit(states, bp, gk, gcand)
         self.ver.slice(k, cand)
         return RoundOut(own, kern, gk, gc, gcand, bp)
 
-    def check_block(self, res, tol):
-        res = _Res(res)
+    def check_block(self, res, tol, sq=None):
         """Block forward outputs: logits, retained IIR states, FIR inputs, block K/V."""
+        res = _Res(res)
         wl = self.wl
         B, C, T, V, d = wl.batch, wl.n_cand, wl.block, wl.vocab, wl.d
-        lg = self.ver.buffer(0, -1, torch.float32, (B, C, T, V)).cpu().numpy()
+        sq = list(range(B)) if sq is None else sq
+        lg = self.ver.buffer(0, -1, torch.float32, (B, C, T, V)).cpu().numpy()[sq]
         e = rel_l2(lg, res.logits)
         assert e <= tol, f"logits rel err {e:.3e}"
         for li, spec in enumerate(wl.layers):
             if spec.kind == "iir":
                 N = spec.param
-                ret = self.ver.buffer(2, li, torch.float32, (B, C, T, d, N, 2)).cpu().numpy()
+                ret = self.ver.buffer(2, li, torch.float32, (B, C, T, d, N, 2)).cpu().numpy()[sq]
                 ref = np.array([[[res.traces[b][c][i][li]["s"] for i in range(T)] for c in range(C)]
-                                for b in range(B)])
+                                for b in range(len(sq))])
                 e = rel_l2(ret, np.stack([ref.real, ref.imag], axis=-1))
                 assert e <= tol, f"layer {li} retained IIR states rel err {e:.3e}"
             elif spec.kind == "fir":
                 Lm1 = spec.param - 1
-                stage = self.ver.buffer(1, li, torch.float32, (B, C, Lm1 + T, d)).cpu().numpy()
+                stage = self.ver.buffer(1, li, torch.float32, (B, C, Lm1 + T, d)).cpu().numpy()[sq]
                 ref = np.array([[[res.traces[b][c][i][li]["v"] for i in range(T)] for c in range(C)]
-                                for b in range(B)])
+                                for b in range(len(sq))])
                 e = rel_l2(stage[:, :, Lm1:], ref)
                 assert e <= tol, f"layer {li} FIR block inputs rel err {e:.3e}"
             elif C > 1:
                 H, dh = spec.param, wl.head_dim
                 tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
-                ks = self.ver.buffer(5, li, tdt, (B, C, H, T, dh)).float().cpu().numpy()
+                ks = self.ver.buffer(5, li, tdt, (B, C, H, T, dh)).float().cpu().numpy()[sq]
                 ref = np.array([[[res.traces[b][c][i][li]["k"] for i in range(T)] for c in range(C)]
-                                for b in range(B)])                       # [B,C,T,H,dh]
+                                for b in range(len(sq))])                 # [B,C,T,H,dh]
                 e = rel_l2(ks, ref.transpose(0, 1, 3, 2, 4))
                 assert e <= tol, f"layer {li} block keys rel err {e:.3e}"
 
