@@ -197,7 +197,9 @@ size_t carve(const evs_config& c, char* base, evs_handle* h) {
         splits_max = std::max(splits_max, (size_t)std::max(pv.splits, pp.splits));
     }
     char* part = take(B * (size_t)g.h_max * splits_max * g.q_max * (dh + 2) * 4);
-    char* gpart = take((size_t)152 * 128 * g.M_max * 4);
+    // split-K partials: splits x tiles <= the CTA target, so splits x N <= target x 128
+    const size_t gpart_floats = (size_t)evs::tc_cta_target() * 128 * g.M_max;
+    char* gpart = take(gpart_floats * 4);
     char* gcnt = take((size_t)(std::max(3 * c.d, c.vocab) / 128 + 1) * 4);
     if (h) {
         h->h = (float*)hbuf;
@@ -206,6 +208,7 @@ size_t carve(const evs_config& c, char* base, evs_handle* h) {
         h->logits = (float*)logits;
         h->attn_part = (float*)part;
         h->gemm_part = (float*)gpart;
+        h->gemm_part_floats = gpart_floats;
         h->gemm_counters = (int*)gcnt;
         h->g = g;
     }

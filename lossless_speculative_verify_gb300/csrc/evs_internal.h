@@ -73,7 +73,8 @@ struct evs_handle {
     float* y;             // [M_max][3d] projection outputs
     float* logits;        // [M_verify][vocab]
     float* attn_part;     // [B][H_max][splits][q_max][dh + 2]
-    float* gemm_part;     // split-K partial sums [<= 152 * 128 * M_max] fp32
+    float* gemm_part;     // split-K partial sums fp32
+    size_t gemm_part_floats;
     int* gemm_counters;   // [max(3d, vocab) / 128] split-K arrival counters
     int tc_smem_max;      // dynamic shared memory the projection kernel may use (bytes)
     evs::AttnPlan plan_verify, plan_prefill;   // tensor-core attention chunking per pass
@@ -106,6 +107,7 @@ void launch_gemm(evs_handle* h, const void* A, const void* W, float* Y, int M, i
 // tcgen05 projection (gemm_tc.cu); false when it cannot take the shape
 bool gemm_tc_supported(int M, int N, int K);
 int gemm_tc_init();
+int tc_cta_target();
 // tcgen05 attention (attn_tc.cu)
 AttnPlan attn_tc_plan(int Q, int B, int H, int t_max, int smem_max);
 int attn_tc_init();

@@ -309,6 +309,8 @@ int gemm_tc_init() {
 // Split K only as far as each CTA still streams at least 8 k-blocks (128 KiB of weights),
 // and no further than filling the 152 SMs once: past that the partial-sum round trip and
 // the per-CTA start-up cost more than the extra parallelism returns.
+int tc_cta_target() { return EVS_TC_CTA_TARGET; }
+
 int tc_splits(int N, int K) {
     const int tiles = N / TC_BM, kblocks = K / TC_BK;
     int s = EVS_TC_CTA_TARGET / tiles;
@@ -324,7 +326,12 @@ struct TcShape {
     size_t smem;
 };
 
-static TcShape tc_shape(int M, int N, int K) {
+// Partial-sum floats a shape needs in global scratch (splits > 1 without the cluster path).
+static size_t tc_part_floats(const TcShape& t, int M, int N) {
+    return (t.splits > 1 && !t.cluster) ? (size_t)t.splits * M * N : 0;
+}
+
+static TcShape tc_shape(int M, int N, int K, size_t part_cap = (size_t)-1, int max_splits = 1 << 30) {
     TcShape t{};
     t.M_for_park = M;
     // tokens padded to the MMA's N granularity; above 256 two accumulators of 256 columns
@@ -332,6 +339,7 @@ static TcShape tc_shape(int M, int N, int K) {
     t.tiles = N / TC_BM;
     t.kblocks = K / TC_BK;
     t.splits = tc_splits(N, K);
+    if (t.splits > max_splits) t.splits = max_splits;
     const int per = (t.kblocks + t.splits - 1) / t.splits;
     t.kbs = EVS_TC_KBS;
     const int kb_bytes = TC_A_BYTES + t.n_pad * 128;
@@ -344,8 +352,22 @@ static TcShape tc_shape(int M, int N, int K) {
     while (t.ncols < t.n_pad) t.ncols <<= 1;
     t.smem = (size_t)t.stages * t.kbs * kb_bytes + 1024 + (2 * t.stages + 1) * 8;
     // cluster reduction when the splits fit a portable cluster and the partial tile fits the ring
-    t.cluster = t.splits > 1 && t.splits <= 8 &&
-                (size_t)t.M_for_park * TC_BM * 4 <= (size_t)t.stages * t.kbs * kb_bytes;
+    // the cluster reduction parks a [M][128] fp32 tile in the ring: deepen the ring (up to
+    // 200 KiB, one CTA per SM) when the default one is too small for it
+    const size_t park = (size_t)t.M_for_park * TC_BM * 4;
+    if (t.splits > 1 && t.splits <= 8 && park > (size_t)t.stages * t.kbs * kb_bytes) {
+        const int need = (int)((park + (size_t)t.kbs * kb_bytes - 1) / ((size_t)t.kbs * kb_bytes));
+        if ((size_t)need * t.kbs * kb_bytes <= 200u * 1024u) {
+            t.stages = need;
+            t.smem = (size_t)t.stages * t.kbs * kb_bytes + 1024 + (2 * t.stages + 1) * 8;
+        }
+    }
+    t.cluster = t.splits > 1 && t.splits <= 8 && park <= (size_t)t.stages * t.kbs * kb_bytes;
+    if (tc_part_floats(t, M, N) > part_cap && t.splits > 1) {
+        // scratch too small for this many partial tiles: fewer splits
+        int s = (int)(part_cap / ((size_t)M * N));
+        return tc_shape(M, N, K, part_cap, s < 1 ? 1 : s);
+    }
     return t;
 }
 
@@ -382,7 +404,7 @@ bool gemm_tc_supported(int M, int N, int K) {
 // Returns false (nothing launched) if a tensor map could not be built.
 bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, float* Y, int M, int N, int K,
                     int ldy, int accumulate) {
-    const TcShape t = tc_shape(M, N, K);
+    const TcShape t = tc_shape(M, N, K, h->gemm_part_floats);
     CUtensorMap ta, tb;
 #if EVS_TC_PACKED
     if (!make_map(&ta, W, (uint64_t)N * K / TC_BK, (uint64_t)TC_BK, TC_BM)) return false;
@@ -445,7 +467,7 @@ extern "C" evs_status evs_projection_noalloc(const void* X, int32_t x_rows, cons
     }
     NoAllocScratch* sc = g_noalloc_ptr[dev];
     const TcShape t = tc_shape(M, N, K);
-    if (t.splits > 1 && (size_t)t.splits * M * N > kNoAllocPartFloats) return EVS_ERR_CAPACITY;
+    if (tc_part_floats(t, M, N) > kNoAllocPartFloats) return EVS_ERR_CAPACITY;
     CUtensorMap ta, tb;
     if (!make_map(&ta, W, (uint64_t)N, (uint64_t)K, TC_BM)) return EVS_ERR_CUDA;
     if (!make_map(&tb, X, (uint64_t)x_rows, (uint64_t)K, (uint32_t)(t.n_pad < 256 ? t.n_pad : 256))) return EVS_ERR_CUDA;
