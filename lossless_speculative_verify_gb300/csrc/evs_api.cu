@@ -185,6 +185,8 @@ size_t carve(const evs_config& c, char* base, evs_handle* h) {
         }
     }
     char* hbuf = take((size_t)g.M_max * d * 4);
+    char* hb = take((size_t)g.M_max * d * 2);
+    char* ssq = take((size_t)(d / 128 + 1) * g.M_max * 4);
     char* act = take((size_t)g.M_max * d * es);
     char* y = take((size_t)g.M_max * 3 * d * 4);
     char* logits = take((size_t)g.M_verify * c.vocab * 4);
@@ -203,6 +205,8 @@ size_t carve(const evs_config& c, char* base, evs_handle* h) {
     char* gcnt = take((size_t)(std::max(3 * c.d, c.vocab) / 128 + 1) * 4);
     if (h) {
         h->h = (float*)hbuf;
+        h->hb = (__nv_bfloat16*)hb;
+        h->ssq = (float*)ssq;
         h->act = act;
         h->y = (float*)y;
         h->logits = (float*)logits;
@@ -263,6 +267,34 @@ void run_layers(evs_handle* h, const int32_t* tokens, int tok_stride, const int3
     const evs_config& c = h->cfg;
     const int d = c.d;
     evs::launch_embed(h, tokens, tok_stride, anchor, p);
+    if (h->fused) {
+        // RMS norm folded into the projections: consumers of h read bf16(h) and scale their
+        // output rows by 1/rms(h); producers of h leave bf16(h) and per-tile sums of squares
+        const evs::GemmFuse in{h->ssq, d / 128, h->g.M_max, d, nullptr, 0, nullptr};
+        const evs::GemmFuse out{nullptr, 0, h->g.M_max, d, h->hb, d, h->ssq};
+        for (int li = 0; li < c.n_layers; ++li) {
+            const evs_layer_weights& W = h->w.layer[li];
+            switch (c.layer_kind[li]) {
+                case EVS_LAYER_FIR:
+                    evs::launch_gemm(h, h->hb, W.w_in, h->y, p.M, d, d, 3 * d, 0, &in);
+                    evs::launch_fir(h, li, p);
+                    evs::launch_gemm(h, h->act, W.w_out, h->h, p.M, d, d, d, 1, &out);
+                    break;
+                case EVS_LAYER_IIR:
+                    evs::launch_gemm(h, h->hb, W.w_in, h->y, p.M, d, d, 3 * d, 0, &in);
+                    evs::launch_iir(h, li, p);
+                    evs::launch_gemm(h, h->act, W.w_out, h->h, p.M, d, d, d, 1, &out);
+                    break;
+                default:
+                    evs::launch_gemm(h, h->hb, W.w_qkv, h->y, p.M, 3 * d, d, 3 * d, 0, &in);
+                    evs::launch_kv_write(h, li, p);
+                    evs::launch_attention(h, li, p);
+                    evs::launch_gemm(h, h->act, W.w_o, h->h, p.M, d, d, d, 1, &out);
+            }
+        }
+        if (with_head) evs::launch_gemm(h, h->hb, h->w.head, h->logits, p.M, c.vocab, d, c.vocab, 0, &in);
+        return;
+    }
     for (int li = 0; li < c.n_layers; ++li) {
         const evs_layer_weights& W = h->w.layer[li];
         evs::launch_rmsnorm(h, p);
@@ -317,6 +349,9 @@ evs_status evs_create(const evs_config* cfg, const evs_weights* weights, void* w
     carve(*cfg, h->ws, h);
     h->tc_smem_max = 0;
     h->pdl = 1;
+    // the norm is folded into the tensor-core projections when every projection shape runs
+    // on them (bf16, widths in whole 128-channel tiles)
+    h->fused = cfg->dtype == EVS_DTYPE_BF16 && cfg->d % 128 == 0 && cfg->vocab % 128 == 0 && h->g.M_max <= 512;
     if (cfg->dtype == EVS_DTYPE_BF16) {
         h->tc_smem_max = evs::gemm_tc_init();
         const int attn_smem = evs::attn_tc_init();

@@ -1,6 +1,7 @@
 // Internal layout of a handle and the kernel launchers it drives.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -43,6 +44,15 @@ struct AttnPlan {
     int smem;        // dynamic shared memory bytes
 };
 
+// Fused-norm extras of one projection (null members are unused).
+struct GemmFuse {
+    const float* ssq_in;     // rows scaled by 1/rms from these per-tile sums of squares
+    int ssq_tiles, ssq_ld, norm_d;
+    __nv_bfloat16* hb_out;   // bf16 copy of the final values
+    int hb_ld;
+    float* ssq_out;          // per-tile sums of squares of the final values
+};
+
 // A pass runs B sequences x C candidates x T block positions; row m = (b*C + c)*T + i.
 struct Pass {
     int B, C, T;        // sequences, candidates, positions per candidate
@@ -73,6 +83,9 @@ struct evs_handle {
     float* y;             // [M_max][3d] projection outputs
     float* logits;        // [M_verify][vocab]
     float* attn_part;     // [B][H_max][splits][q_max][dh + 2]
+    int fused;            // norm folded into the projections (bf16, all shapes on tcgen05)
+    __nv_bfloat16* hb;    // [M_max][d] bf16 copy of the residual stream (fused path)
+    float* ssq;           // [d / 128][M_max] per-tile sums of squares of h (fused path)
     float* gemm_part;     // split-K partial sums fp32
     size_t gemm_part_floats;
     int* gemm_counters;   // [max(3d, vocab) / 128] split-K arrival counters
@@ -103,7 +116,7 @@ void launch_embed(evs_handle* h, const int32_t* tokens, int tok_stride_bc, const
                   const Pass& p);
 void launch_rmsnorm(evs_handle* h, const Pass& p);
 void launch_gemm(evs_handle* h, const void* A, const void* W, float* Y, int M, int N, int K,
-                 int ldy, int accumulate);
+                 int ldy, int accumulate, const GemmFuse* fz = nullptr);
 // tcgen05 projection (gemm_tc.cu); false when it cannot take the shape
 bool gemm_tc_supported(int M, int N, int K);
 int gemm_tc_init();
@@ -113,7 +126,7 @@ AttnPlan attn_tc_plan(int Q, int B, int H, int t_max, int smem_max);
 int attn_tc_init();
 bool launch_attn_tc(evs_handle* h, int layer, const Pass& p, const AttnPlan& plan);
 bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, float* Y, int M, int N,
-                    int K, int ldy, int accumulate);
+                    int K, int ldy, int accumulate, const GemmFuse* fz = nullptr);
 void launch_fir(evs_handle* h, int layer, const Pass& p);
 void launch_iir(evs_handle* h, int layer, const Pass& p);
 void launch_kv_write(evs_handle* h, int layer, const Pass& p);

@@ -49,6 +49,13 @@ struct TcArgs {
     float* part;      // [splits][M][N] partial sums when splits > 1
     int* counters;    // [N / 128] arrival counters, zero between launches
     uint32_t* flags;
+    // fused RMS norm: rows of the product scaled by 1/rms(h) from the producer's per-tile
+    // sums of squares; the final writer of h leaves bf16(h) and its own sums of squares
+    const float* ssq_in;   // [ssq_tiles][ssq_ld] or null
+    int ssq_tiles, ssq_ld, norm_d;
+    __nv_bfloat16* hb_out; // [M][hb_ld] or null
+    int hb_ld;
+    float* ssq_out;        // [N / 128][ssq_ld] or null
 };
 
 __global__ void __launch_bounds__(128, 2)
@@ -57,6 +64,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     __shared__ uint32_t tmem_slot[1];
     __shared__ volatile int abort_flag[1];
     __shared__ int last_flag[1];
+    __shared__ float rinv_s[512];
+    __shared__ float red_s[4 * 512];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const int b_bytes = p.n_pad * 128;
@@ -172,50 +181,70 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tc_fence_after();
     const bool bad = !ok || *abort_flag;
     if (bad && threadIdx.x == 0) atomicOr(p.flags, (uint32_t)EVS_FLAG_TIMEOUT);
-    const int n = n0 + warp * 32 + lane;
+    if (p.ssq_in) {  // 1/rms of each token row, from the per-tile sums of squares of h
+        for (int m = threadIdx.x; m < p.M; m += blockDim.x) {
+            float ss = 0.f;
+            for (int t = 0; t < p.ssq_tiles; ++t) ss += p.ssq_in[(size_t)t * p.ssq_ld + m];
+            rinv_s[m] = rsqrtf(ss / (float)p.norm_d + 1e-6f);
+        }
+    }
+    __syncthreads();
+    // One output value: row scale, store (or accumulate into the residual), bf16 copy, and
+    // this warp's share of the row's sum of squares. All lanes of a warp call it for the
+    // same m with consecutive channels nl.
+    auto finish = [&](int m, int nl, float v, bool live) {
+        if (p.ssq_in) v *= rinv_s[m];
+        float out = v;
+        if (live) {
+            float* dst = p.Y + (size_t)m * p.ldy + n0 + nl;
+            if (p.accumulate) out += *dst;
+            *dst = out;
+            if (p.hb_out) p.hb_out[(size_t)m * p.hb_ld + n0 + nl] = __float2bfloat16_rn(out);
+        }
+        if (p.ssq_out) {
+            const float sq = warp_sum(live ? out * out : 0.f);
+            if ((nl & 31) == 0) red_s[(nl >> 5) * 512 + m] = sq;
+        }
+    };
+    int own_lo = 0, own_hi = 0;   // token rows whose sums of squares this CTA completes
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    const bool col_ok = n < p.N && !bad;
+    const int nl_lane = warp * 32 + lane;
     if (p.splits == 1) {
         for (int c0 = 0; c0 < p.M; c0 += 16) {
             float v[16];
             tmem_ld16(trow + (uint32_t)c0, v);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int m = c0 + j;
-                if (m < p.M && col_ok) {
-                    float* dst = p.Y + (size_t)m * p.ldy + n;
-                    *dst = p.accumulate ? (*dst + v[j]) : v[j];
-                }
-            }
+            for (int j = 0; j < 16; ++j)
+                if (c0 + j < p.M) finish(c0 + j, nl_lane, v[j], !bad);
         }
+        own_hi = p.M;
     } else if (p.cluster) {
         // split-K through distributed shared memory: every CTA of the cluster parks its
         // partial tile [M][128] in its own (now idle) ring, then CTA r sums its share of the
-        // token columns across the cluster in a fixed order and writes them out
+        // token rows across the cluster in a fixed order and finishes them
         float* park = reinterpret_cast<float*>(smem);
         for (int c0 = 0; c0 < p.M; c0 += 16) {
             float v[16];
             tmem_ld16(trow + (uint32_t)c0, v);
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                if (c0 + j < p.M) park[(size_t)(c0 + j) * TC_BM + warp * 32 + lane] = v[j];
+                if (c0 + j < p.M) park[(size_t)(c0 + j) * TC_BM + nl_lane] = v[j];
         }
         cluster_sync();
         const int r = split;                      // rank in the cluster (cluster spans y)
-        const int m_lo = (int)((long long)p.M * r / p.splits), m_hi = (int)((long long)p.M * (r + 1) / p.splits);
+        own_lo = (int)((long long)p.M * r / p.splits);
+        own_hi = (int)((long long)p.M * (r + 1) / p.splits);
         const uint32_t base = smem_u32(park);
         const int ch = threadIdx.x;               // channel within the tile
-        for (int m = m_lo; m < m_hi; ++m) {
+        for (int m = own_lo; m < own_hi; ++m) {
             const uint32_t off = base + (uint32_t)(m * TC_BM + ch) * 4u;
             float acc = 0.f;
             for (int sp = 0; sp < p.splits; ++sp) acc += ld_peer_f32(map_peer(off, (uint32_t)sp));
-            if (!bad && n0 + ch < p.N) {
-                float* dst = p.Y + (size_t)m * p.ldy + n0 + ch;
-                *dst = p.accumulate ? (*dst + acc) : acc;
-            }
+            finish(m, ch, acc, !bad);
         }
         cluster_sync();                           // peers finished reading this CTA's park
     } else {
+        const int n = n0 + nl_lane;
         float* mine = p.part + (size_t)split * p.M * p.N;
         for (int c0 = 0; c0 < p.M; c0 += 16) {
             float v[16];
@@ -223,7 +252,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int m = c0 + j;
-                if (m < p.M && col_ok) mine[(size_t)m * p.N + n] = v[j];
+                if (m < p.M && !bad) mine[(size_t)m * p.N + n] = v[j];
             }
         }
         __threadfence();
@@ -232,28 +261,30 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         __syncthreads();
         if (*last_flag) {
             __threadfence();
-            if (col_ok) {
-                // four rows at a time, every split's value requested before any is summed
-                for (int m0 = 0; m0 < p.M; m0 += 4) {
-                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                    for (int sp = 0; sp < p.splits; ++sp) {
-                        float v[4];
+            // four rows at a time, every split's value requested before any is summed
+            for (int m0 = 0; m0 < p.M; m0 += 4) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int sp = 0; sp < p.splits; ++sp) {
+                    float v[4];
 #pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            v[u] = (m0 + u < p.M) ? __ldcg(p.part + ((size_t)sp * p.M + m0 + u) * p.N + n) : 0.f;
+                    for (int u = 0; u < 4; ++u)
+                        v[u] = (m0 + u < p.M) ? __ldcg(p.part + ((size_t)sp * p.M + m0 + u) * p.N + n) : 0.f;
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) acc[u] += v[u];
-                    }
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        if (m0 + u >= p.M) break;
-                        float* dst = p.Y + (size_t)(m0 + u) * p.ldy + n;
-                        *dst = p.accumulate ? (*dst + acc[u]) : acc[u];
-                    }
+                    for (int u = 0; u < 4; ++u) acc[u] += v[u];
                 }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (m0 + u < p.M) finish(m0 + u, nl_lane, acc[u], !bad);
             }
             if (threadIdx.x == 0) p.counters[tile] = 0;
+            own_hi = p.M;
         }
+    }
+    if (p.ssq_out) {
+        __syncthreads();
+        for (int m = own_lo + threadIdx.x; m < own_hi; m += blockDim.x)
+            p.ssq_out[(size_t)tile * p.ssq_ld + m] =
+                red_s[m] + red_s[512 + m] + red_s[1024 + m] + red_s[1536 + m];
     }
     tc_fence_before();
     __syncthreads();
@@ -403,7 +434,7 @@ bool gemm_tc_supported(int M, int N, int K) {
 
 // Returns false (nothing launched) if a tensor map could not be built.
 bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, float* Y, int M, int N, int K,
-                    int ldy, int accumulate) {
+                    int ldy, int accumulate, const GemmFuse* fz) {
     const TcShape t = tc_shape(M, N, K, h->gemm_part_floats);
     CUtensorMap ta, tb;
 #if EVS_TC_PACKED
@@ -414,7 +445,16 @@ bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, flo
     if (!make_map(&tb, X, (uint64_t)x_rows, (uint64_t)K, (uint32_t)(t.n_pad < 256 ? t.n_pad : 256))) return false;
     if ((int)t.smem > h->tc_smem_max) return false;
     TcArgs a{Y, ldy, M, N, t.kblocks, t.splits, t.n_pad, t.stages, accumulate, t.ncols, t.kbs, t.cluster,
-             h->gemm_part, h->gemm_counters, h->flags};
+             h->gemm_part, h->gemm_counters, h->flags, nullptr, 0, 0, 0, nullptr, 0, nullptr};
+    if (fz) {
+        a.ssq_in = fz->ssq_in;
+        a.ssq_tiles = fz->ssq_tiles;
+        a.ssq_ld = fz->ssq_ld;
+        a.norm_d = fz->norm_d;
+        a.hb_out = fz->hb_out;
+        a.hb_ld = fz->hb_ld;
+        a.ssq_out = fz->ssq_out;
+    }
     return launch_tc(t, ta, tb, a, h->stream, h->pdl != 0);
 }
 
@@ -476,7 +516,7 @@ extern "C" evs_status evs_projection_noalloc(const void* X, int32_t x_rows, cons
     // the array keeps the previous call's contents: the counters must start at zero
     if (cudaMemsetAsync(sc->counters, 0, sizeof(sc->counters), s) != cudaSuccess) return EVS_ERR_CUDA;
     TcArgs a{Y, ldy, M, N, t.kblocks, t.splits, t.n_pad, t.stages, accumulate, t.ncols, t.kbs, t.cluster,
-             sc->part, sc->counters, &sc->flags};
+             sc->part, sc->counters, &sc->flags, nullptr, 0, 0, 0, nullptr, 0, nullptr};
     if (!launch_tc(t, ta, tb, a, s, false)) return EVS_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? EVS_OK : EVS_ERR_CUDA;
 }

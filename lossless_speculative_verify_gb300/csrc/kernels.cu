@@ -17,7 +17,9 @@ __global__ void embed_kernel(const T* __restrict__ E, const int32_t* __restrict_
                              int tok_stride_bc, const int32_t* __restrict__ anchor,
                              float* __restrict__ h, int d, int C, int Tb, int vocab, int B,
                              const int32_t* __restrict__ kv_len, int32_t* __restrict__ kv_base,
-                             uint32_t* __restrict__ flags) {
+                             uint32_t* __restrict__ flags, __nv_bfloat16* __restrict__ hb,
+                             float* __restrict__ ssq, int ssq_tiles, int ssq_ld) {
+    __shared__ float red[32];
     pdl_trigger();
     pdl_wait();
     const int m = blockIdx.x;
@@ -29,7 +31,17 @@ __global__ void embed_kernel(const T* __restrict__ E, const int32_t* __restrict_
     }
     const T* row = E + (size_t)tok * d;
     float* out = h + (size_t)m * d;
-    for (int c = threadIdx.x; c < d; c += blockDim.x) out[c] = to_f32(row[c]);
+    float ss = 0.f;
+    for (int c = threadIdx.x; c < d; c += blockDim.x) {
+        const float v = to_f32(row[c]);
+        out[c] = v;
+        ss += v * v;
+        if (hb) hb[(size_t)m * d + c] = __float2bfloat16_rn(v);
+    }
+    if (ssq) {  // the row's sum of squares in tile slot 0, the other slots cleared
+        ss = block_sum(ss, red);
+        for (int t = threadIdx.x; t < ssq_tiles; t += blockDim.x) ssq[(size_t)t * ssq_ld + m] = t == 0 ? ss : 0.f;
+    }
     if (m == 0)
         for (int j = threadIdx.x; j < B; j += blockDim.x) kv_base[j] = kv_len[j];
 }
@@ -705,10 +717,12 @@ void launch_embed(evs_handle* h, const int32_t* tokens, int tok_stride_bc, const
     const int d = h->cfg.d;
     if (is_bf16(h))
         launch_k(h, embed_kernel<bf16>, dim3(p.M), dim3(256), 0, (const bf16*)h->w.embed, tokens, tok_stride_bc,
-            anchor, h->h, d, p.C, p.T, h->cfg.vocab, p.B, h->kv_len, h->kv_base, h->flags);
+            anchor, h->h, d, p.C, p.T, h->cfg.vocab, p.B, h->kv_len, h->kv_base, h->flags,
+            h->fused ? h->hb : nullptr, h->fused ? h->ssq : nullptr, d / 128, h->g.M_max);
     else
         launch_k(h, embed_kernel<float>, dim3(p.M), dim3(256), 0, (const float*)h->w.embed, tokens, tok_stride_bc,
-            anchor, h->h, d, p.C, p.T, h->cfg.vocab, p.B, h->kv_len, h->kv_base, h->flags);
+            anchor, h->h, d, p.C, p.T, h->cfg.vocab, p.B, h->kv_len, h->kv_base, h->flags,
+            (__nv_bfloat16*)nullptr, (float*)nullptr, 0, 0);
     h->launches++;
     prof_end(h, EVS_K_EMBED);
 }
@@ -723,10 +737,10 @@ void launch_rmsnorm(evs_handle* h, const Pass& p) {
 }
 
 void launch_gemm(evs_handle* h, const void* A, const void* W, float* Y, int M, int N, int K, int ldy,
-                 int accumulate) {
+                 int accumulate, const GemmFuse* fz) {
     prof_begin(h, EVS_K_GEMM);
     if (is_bf16(h) && gemm_tc_supported(M, N, K) &&
-        launch_gemm_tc(h, A, h->g.M_max, W, Y, M, N, K, ldy, accumulate)) {
+        launch_gemm_tc(h, A, h->g.M_max, W, Y, M, N, K, ldy, accumulate, fz)) {
         h->launches++;
         prof_end(h, EVS_K_GEMM);
         return;
