@@ -176,18 +176,31 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     // ---- epilogue: lane = output channel, columns = tokens ---------------------------------
     pdl_wait();
+    if (p.ssq_in && warp >= 2) {
+        // 1/rms of each token row from the per-tile sums of squares of h, computed by the two
+        // warps that are idle during the mainloop: a row's tiles are spread over the lanes,
+        // eight rows' loads in flight before any is reduced
+        for (int m0 = (warp - 2) * 8; m0 < p.M; m0 += 16) {
+            float part[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                float ss = 0.f;
+                if (m0 + u < p.M)
+                    for (int t = lane; t < p.ssq_tiles; t += 32) ss += p.ssq_in[(size_t)t * p.ssq_ld + m0 + u];
+                part[u] = ss;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float ss = warp_sum(part[u]);
+                if (lane == 0 && m0 + u < p.M) rinv_s[m0 + u] = rsqrtf(ss / (float)p.norm_d + 1e-6f);
+            }
+        }
+    }
     __syncwarp();
     const bool ok = mbar_wait(done, 0);
     tc_fence_after();
     const bool bad = !ok || *abort_flag;
     if (bad && threadIdx.x == 0) atomicOr(p.flags, (uint32_t)EVS_FLAG_TIMEOUT);
-    if (p.ssq_in) {  // 1/rms of each token row, from the per-tile sums of squares of h
-        for (int m = threadIdx.x; m < p.M; m += blockDim.x) {
-            float ss = 0.f;
-            for (int t = 0; t < p.ssq_tiles; ++t) ss += p.ssq_in[(size_t)t * p.ssq_ld + m];
-            rinv_s[m] = rsqrtf(ss / (float)p.norm_d + 1e-6f);
-        }
-    }
     __syncthreads();
     // One output value: row scale, store (or accumulate into the residual), bf16 copy, and
     // this warp's share of the row's sum of squares. All lanes of a warp call it for the
@@ -384,8 +397,14 @@ static TcShape tc_shape(int M, int N, int K, size_t part_cap = (size_t)-1, int m
     t.smem = (size_t)t.stages * t.kbs * kb_bytes + 1024 + (2 * t.stages + 1) * 8;
     // cluster reduction when the splits fit a portable cluster and the partial tile fits the ring
     // the cluster reduction parks a [M][128] fp32 tile in the ring: deepen the ring (up to
-    // 200 KiB, one CTA per SM) when the default one is too small for it
+    // 200 KiB, one CTA per SM) when the default one is too small for it, and then split
+    // only as far as one CTA per SM fills the GPU once
     const size_t park = (size_t)t.M_for_park * TC_BM * 4;
+    if (t.splits > 1 && park > (size_t)t.stages * t.kbs * kb_bytes && max_splits == (1 << 30)) {
+        int s1 = 152 / t.tiles;
+        if (s1 < 1) s1 = 1;
+        if (s1 < t.splits) return tc_shape(M, N, K, part_cap, s1);
+    }
     if (t.splits > 1 && t.splits <= 8 && park > (size_t)t.stages * t.kbs * kb_bytes) {
         const int need = (int)((park + (size_t)t.kbs * kb_bytes - 1) / ((size_t)t.kbs * kb_bytes));
         if ((size_t)need * t.kbs * kb_bytes <= 200u * 1024u) {

@@ -135,20 +135,29 @@ __global__ void fir_kernel(const float* __restrict__ Y, int ldy, T* __restrict__
     float* st = stage + (size_t)bc * srows * d;
     if (!commit)
         for (int j = 0; j < L - 1; ++j) st[(size_t)j * d + ch] = hist[j];
-    for (int i = 0; i < Tb; ++i) {
-        const size_t m = (size_t)bc * Tb + i;
-        const float v = Y[m * ldy + ch];
-        float y = w[0] * v;
-        // hist[L-2] = v_{t-1}, ..., hist[0] = v_{t-L+1}
+    for (int i0 = 0; i0 < Tb; i0 += 8) {
+        float vin[8];   // eight positions' inputs requested before any is used
 #pragma unroll
-        for (int j = 1; j < 16; ++j)
-            if (j < L) y = fmaf(w[j], hist[L - 1 - j], y);
+        for (int u = 0; u < 8; ++u)
+            vin[u] = (i0 + u < Tb) ? Y[((size_t)bc * Tb + i0 + u) * ldy + ch] : 0.f;
 #pragma unroll
-        for (int j = 0; j < 15; ++j)
-            if (j < L - 2) hist[j] = hist[j + 1];
-        hist[L - 2] = v;
-        out[m * d + ch] = from_f32<T>(y);
-        if (!commit) st[(size_t)(L - 1 + i) * d + ch] = v;
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u;
+            if (i >= Tb) break;
+            const size_t m = (size_t)bc * Tb + i;
+            const float v = vin[u];
+            float y = w[0] * v;
+            // hist[L-2] = v_{t-1}, ..., hist[0] = v_{t-L+1}
+#pragma unroll
+            for (int j = 1; j < 16; ++j)
+                if (j < L) y = fmaf(w[j], hist[L - 1 - j], y);
+#pragma unroll
+            for (int j = 0; j < 15; ++j)
+                if (j < L - 2) hist[j] = hist[j + 1];
+            hist[L - 2] = v;
+            out[m * d + ch] = from_f32<T>(y);
+            if (!commit) st[(size_t)(L - 1 + i) * d + ch] = v;
+        }
     }
     if (commit)
         for (int j = 0; j < L - 1; ++j) tail[((size_t)b * (L - 1) + j) * d + ch] = hist[j];
@@ -173,16 +182,24 @@ __global__ void iir_kernel(const float* __restrict__ Y, int ldy, T* __restrict__
     const int ch = g / N, n = g % N;
     const float2 l = lam[g], bq = bb[g], cq = cc[g];
     float2 s = state[(size_t)b * d * N + g];
-    for (int i = 0; i < Tb; ++i) {
-        const size_t m = (size_t)bc * Tb + i;
-        const float u = Y[m * ldy + ch];
-        const float sx = fmaf(l.x, s.x, fmaf(-l.y, s.y, bq.x * u));
-        const float sy = fmaf(l.x, s.y, fmaf(l.y, s.x, bq.y * u));
-        s = make_float2(sx, sy);
-        float part = fmaf(cq.x, s.x, -cq.y * s.y);
-        for (int o = N >> 1; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-        if (n == 0) out[m * d + ch] = from_f32<T>(part);
-        if (!commit) ret[((size_t)bc * Tb + i) * d * N + g] = s;
+    for (int i0 = 0; i0 < Tb; i0 += 8) {
+        float uin[8];   // eight positions' inputs requested before any is used
+#pragma unroll
+        for (int k = 0; k < 8; ++k) uin[k] = (i0 + k < Tb) ? Y[((size_t)bc * Tb + i0 + k) * ldy + ch] : 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = i0 + k;
+            if (i >= Tb) break;
+            const size_t m = (size_t)bc * Tb + i;
+            const float u = uin[k];
+            const float sx = fmaf(l.x, s.x, fmaf(-l.y, s.y, bq.x * u));
+            const float sy = fmaf(l.x, s.y, fmaf(l.y, s.x, bq.y * u));
+            s = make_float2(sx, sy);
+            float part = fmaf(cq.x, s.x, -cq.y * s.y);
+            for (int o = N >> 1; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            if (n == 0) out[m * d + ch] = from_f32<T>(part);
+            if (!commit) ret[((size_t)bc * Tb + i) * d * N + g] = s;
+        }
     }
     if (commit) state[(size_t)b * d * N + g] = s;
 }
@@ -760,13 +777,13 @@ void launch_fir(evs_handle* h, int li, const Pass& p) {
     prof_begin(h, EVS_K_FIR);
     const int d = h->cfg.d;
     const LayerDesc& L = h->layer[li];
-    dim3 grid((d + 127) / 128, p.B * p.C);
+    dim3 grid((d + 63) / 64, p.B * p.C);
     const float* taps = h->w.layer[li].fir_taps;
     if (is_bf16(h))
-        launch_k(h, fir_kernel<bf16>, dim3(grid), dim3(128), 0, h->y, 3 * d, (bf16*)h->act, d, p.C, p.T, p.commit, taps,
+        launch_k(h, fir_kernel<bf16>, dim3(grid), dim3(64), 0, h->y, 3 * d, (bf16*)h->act, d, p.C, p.T, p.commit, taps,
                                                        L.param, L.tail, L.stage);
     else
-        launch_k(h, fir_kernel<float>, dim3(grid), dim3(128), 0, h->y, 3 * d, (float*)h->act, d, p.C, p.T, p.commit,
+        launch_k(h, fir_kernel<float>, dim3(grid), dim3(64), 0, h->y, 3 * d, (float*)h->act, d, p.C, p.T, p.commit,
                                                         taps, L.param, L.tail, L.stage);
     h->launches++;
     prof_end(h, EVS_K_FIR);
