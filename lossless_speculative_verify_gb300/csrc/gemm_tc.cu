@@ -28,8 +28,11 @@ constexpr int TC_A_BYTES = TC_BM * TC_BK * 2; // 16 KiB
 #ifndef EVS_TC_CTA_TARGET
 #define EVS_TC_CTA_TARGET 304  // CTAs one projection aims to fill (two per SM)
 #endif
+#ifndef EVS_TC_MAX_SPLITS
+#define EVS_TC_MAX_SPLITS 8
+#endif
 #ifndef EVS_TC_MIN_KB
-#define EVS_TC_MIN_KB 8        // fewest 64-wide k-blocks a split may stream
+#define EVS_TC_MIN_KB 2        // fewest 64-wide k-blocks a split may stream
 #endif
 constexpr int TC_SMEM_BUDGET = EVS_TC_SMEM_KB * 1024;
 #ifndef EVS_TC_KBS
@@ -46,6 +49,7 @@ struct TcArgs {
     float* Y;
     int ldy, M, N, kblocks, splits, n_pad, stages, accumulate, ncols, kbs;
     int cluster;      // 1: the splits of a tile form a cluster and reduce through DSMEM
+    int park_rows;    // token rows parked per round of the cluster reduction
     float* part;      // [splits][M][N] partial sums when splits > 1
     int* counters;    // [N / 128] arrival counters, zero between launches
     uint32_t* flags;
@@ -232,30 +236,33 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         own_hi = p.M;
     } else if (p.cluster) {
-        // split-K through distributed shared memory: every CTA of the cluster parks its
-        // partial tile [M][128] in its own (now idle) ring, then CTA r sums its share of the
-        // token rows across the cluster in a fixed order and finishes them
+        // split-K through distributed shared memory: the CTAs of the cluster park their
+        // partial tiles in their own (now idle) rings, a chunk of token rows at a time; CTA r
+        // sums its share of each chunk's rows across the cluster in a fixed order
         float* park = reinterpret_cast<float*>(smem);
-        for (int c0 = 0; c0 < p.M; c0 += 16) {
-            float v[16];
-            tmem_ld16(trow + (uint32_t)c0, v);
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                if (c0 + j < p.M) park[(size_t)(c0 + j) * TC_BM + nl_lane] = v[j];
-        }
-        cluster_sync();
-        const int r = split;                      // rank in the cluster (cluster spans y)
-        own_lo = (int)((long long)p.M * r / p.splits);
-        own_hi = (int)((long long)p.M * (r + 1) / p.splits);
         const uint32_t base = smem_u32(park);
         const int ch = threadIdx.x;               // channel within the tile
-        for (int m = own_lo; m < own_hi; ++m) {
-            const uint32_t off = base + (uint32_t)(m * TC_BM + ch) * 4u;
-            float acc = 0.f;
-            for (int sp = 0; sp < p.splits; ++sp) acc += ld_peer_f32(map_peer(off, (uint32_t)sp));
-            finish(m, ch, acc, !bad);
+        const int r = split;                      // rank in the cluster (cluster spans y)
+        for (int c_lo = 0; c_lo < p.M; c_lo += p.park_rows) {
+            const int cnt = min(p.park_rows, p.M - c_lo);
+            for (int c0 = 0; c0 < cnt; c0 += 16) {
+                float v[16];
+                tmem_ld16(trow + (uint32_t)(c_lo + c0), v);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (c0 + j < cnt) park[(size_t)(c0 + j) * TC_BM + nl_lane] = v[j];
+            }
+            cluster_sync();
+            const int lo = c_lo + (int)((long long)cnt * r / p.splits);
+            const int hi = c_lo + (int)((long long)cnt * (r + 1) / p.splits);
+            for (int m = lo; m < hi; ++m) {
+                const uint32_t off = base + (uint32_t)((m - c_lo) * TC_BM + ch) * 4u;
+                float acc = 0.f;
+                for (int sp = 0; sp < p.splits; ++sp) acc += ld_peer_f32(map_peer(off, (uint32_t)sp));
+                finish(m, ch, acc, !bad);
+            }
+            cluster_sync();                       // peers finished reading this chunk
         }
-        cluster_sync();                           // peers finished reading this CTA's park
     } else {
         const int n = n0 + nl_lane;
         float* mine = p.part + (size_t)split * p.M * p.N;
@@ -295,9 +302,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     if (p.ssq_out) {
         __syncthreads();
-        for (int m = own_lo + threadIdx.x; m < own_hi; m += blockDim.x)
-            p.ssq_out[(size_t)tile * p.ssq_ld + m] =
-                red_s[m] + red_s[512 + m] + red_s[1024 + m] + red_s[1536 + m];
+        auto put = [&](int lo, int hi) {
+            for (int m = lo + threadIdx.x; m < hi; m += blockDim.x)
+                p.ssq_out[(size_t)tile * p.ssq_ld + m] =
+                    red_s[m] + red_s[512 + m] + red_s[1024 + m] + red_s[1536 + m];
+        };
+        if (p.splits > 1 && p.cluster) {
+            for (int c_lo = 0; c_lo < p.M; c_lo += p.park_rows) {
+                const int cnt = min(p.park_rows, p.M - c_lo);
+                put(c_lo + (int)((long long)cnt * split / p.splits),
+                    c_lo + (int)((long long)cnt * (split + 1) / p.splits));
+            }
+        } else {
+            put(own_lo, own_hi);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -359,6 +377,7 @@ int tc_splits(int N, int K) {
     const int tiles = N / TC_BM, kblocks = K / TC_BK;
     int s = EVS_TC_CTA_TARGET / tiles;
     if (s > kblocks / EVS_TC_MIN_KB) s = kblocks / EVS_TC_MIN_KB;
+    if (s > EVS_TC_MAX_SPLITS) s = EVS_TC_MAX_SPLITS;   // stay within one portable cluster
     if (s < 1) s = 1;
     return s;
 }
@@ -366,7 +385,7 @@ int tc_splits(int N, int K) {
 // Launch shape of one projection: token padding, split-K, k-blocks per stage, ring depth,
 // TMEM columns and dynamic shared memory.
 struct TcShape {
-    int n_pad, tiles, kblocks, splits, kbs, stages, ncols, cluster, M_for_park;
+    int n_pad, tiles, kblocks, splits, kbs, stages, ncols, cluster, M_for_park, park_rows;
     size_t smem;
 };
 
@@ -396,23 +415,10 @@ static TcShape tc_shape(int M, int N, int K, size_t part_cap = (size_t)-1, int m
     while (t.ncols < t.n_pad) t.ncols <<= 1;
     t.smem = (size_t)t.stages * t.kbs * kb_bytes + 1024 + (2 * t.stages + 1) * 8;
     // cluster reduction when the splits fit a portable cluster and the partial tile fits the ring
-    // the cluster reduction parks a [M][128] fp32 tile in the ring: deepen the ring (up to
-    // 200 KiB, one CTA per SM) when the default one is too small for it, and then split
-    // only as far as one CTA per SM fills the GPU once
-    const size_t park = (size_t)t.M_for_park * TC_BM * 4;
-    if (t.splits > 1 && park > (size_t)t.stages * t.kbs * kb_bytes && max_splits == (1 << 30)) {
-        int s1 = 152 / t.tiles;
-        if (s1 < 1) s1 = 1;
-        if (s1 < t.splits) return tc_shape(M, N, K, part_cap, s1);
-    }
-    if (t.splits > 1 && t.splits <= 8 && park > (size_t)t.stages * t.kbs * kb_bytes) {
-        const int need = (int)((park + (size_t)t.kbs * kb_bytes - 1) / ((size_t)t.kbs * kb_bytes));
-        if ((size_t)need * t.kbs * kb_bytes <= 200u * 1024u) {
-            t.stages = need;
-            t.smem = (size_t)t.stages * t.kbs * kb_bytes + 1024 + (2 * t.stages + 1) * 8;
-        }
-    }
-    t.cluster = t.splits > 1 && t.splits <= 8 && park <= (size_t)t.stages * t.kbs * kb_bytes;
+    // the cluster reduction parks [rows][128] fp32 partial tiles in the ring, as many token
+    // rows at a time as fit (a multiple of 16)
+    t.park_rows = (int)(((size_t)t.stages * t.kbs * kb_bytes / (TC_BM * 4)) / 16 * 16);
+    t.cluster = t.splits > 1 && t.splits <= 8 && t.park_rows >= 16;
     if (tc_part_floats(t, M, N) > part_cap && t.splits > 1) {
         // scratch too small for this many partial tiles: fewer splits
         int s = (int)(part_cap / ((size_t)M * N));
@@ -464,7 +470,7 @@ bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, flo
     if (!make_map(&tb, X, (uint64_t)x_rows, (uint64_t)K, (uint32_t)(t.n_pad < 256 ? t.n_pad : 256))) return false;
     if ((int)t.smem > h->tc_smem_max) return false;
     TcArgs a{Y, ldy, M, N, t.kblocks, t.splits, t.n_pad, t.stages, accumulate, t.ncols, t.kbs, t.cluster,
-             h->gemm_part, h->gemm_counters, h->flags, nullptr, 0, 0, 0, nullptr, 0, nullptr};
+             t.park_rows, h->gemm_part, h->gemm_counters, h->flags, nullptr, 0, 0, 0, nullptr, 0, nullptr};
     if (fz) {
         a.ssq_in = fz->ssq_in;
         a.ssq_tiles = fz->ssq_tiles;
@@ -535,7 +541,7 @@ extern "C" evs_status evs_projection_noalloc(const void* X, int32_t x_rows, cons
     // the array keeps the previous call's contents: the counters must start at zero
     if (cudaMemsetAsync(sc->counters, 0, sizeof(sc->counters), s) != cudaSuccess) return EVS_ERR_CUDA;
     TcArgs a{Y, ldy, M, N, t.kblocks, t.splits, t.n_pad, t.stages, accumulate, t.ncols, t.kbs, t.cluster,
-             sc->part, sc->counters, &sc->flags, nullptr, 0, 0, 0, nullptr, 0, nullptr};
+             t.park_rows, sc->part, sc->counters, &sc->flags, nullptr, 0, 0, 0, nullptr, 0, nullptr};
     if (!launch_tc(t, ta, tb, a, s, false)) return EVS_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? EVS_OK : EVS_ERR_CUDA;
 }
