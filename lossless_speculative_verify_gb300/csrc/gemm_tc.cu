@@ -255,11 +255,22 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             cluster_sync();
             const int lo = c_lo + (int)((long long)cnt * r / p.splits);
             const int hi = c_lo + (int)((long long)cnt * (r + 1) / p.splits);
-            for (int m = lo; m < hi; ++m) {
-                const uint32_t off = base + (uint32_t)((m - c_lo) * TC_BM + ch) * 4u;
-                float acc = 0.f;
-                for (int sp = 0; sp < p.splits; ++sp) acc += ld_peer_f32(map_peer(off, (uint32_t)sp));
-                finish(m, ch, acc, !bad);
+            for (int m = lo; m < hi; m += 8) {   // eight rows' peer loads in flight at once
+                float acc[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) acc[u] = 0.f;
+                for (int sp = 0; sp < p.splits; ++sp) {
+                    const uint32_t peer = map_peer(base, (uint32_t)sp);
+                    float v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        v[u] = (m + u < hi) ? ld_peer_f32(peer + (uint32_t)((m + u - c_lo) * TC_BM + ch) * 4u) : 0.f;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) acc[u] += v[u];
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (m + u < hi) finish(m + u, ch, acc[u], !bad);
             }
             cluster_sync();                       // peers finished reading this chunk
         }
@@ -377,7 +388,9 @@ int tc_splits(int N, int K) {
     const int tiles = N / TC_BM, kblocks = K / TC_BK;
     int s = EVS_TC_CTA_TARGET / tiles;
     if (s > kblocks / EVS_TC_MIN_KB) s = kblocks / EVS_TC_MIN_KB;
-    if (s > EVS_TC_MAX_SPLITS) s = EVS_TC_MAX_SPLITS;   // stay within one portable cluster
+    // stay within one portable cluster unless that leaves most SMs idle (narrow outputs such
+    // as the LM head), where the global partial-sum path splits further
+    if (s > EVS_TC_MAX_SPLITS && tiles * EVS_TC_MAX_SPLITS >= 152) s = EVS_TC_MAX_SPLITS;
     if (s < 1) s = 1;
     return s;
 }

@@ -24,8 +24,8 @@ def ver():
     build()
     from lossless_speculative_verify_gb300 import DeviceWeights, Verifier, make_config
     from synth import LayerSpec, gen_weights, get_workload
-    wl = get_workload("d1024_l8_p8k_bf16").replace(
-        layers=(LayerSpec("fir", 3), LayerSpec("attn", 8)), batch=4, prefill_chunk=128)
+    wl = get_workload("d4096_l32_p8k_bf16").replace(
+        layers=(LayerSpec("fir", 3),), batch=4, prefill_chunk=128)
     layers = [(s.kind, s.param) for s in wl.layers]
     cfg = make_config(wl.d, layers, wl.head_dim, wl.gamma, wl.batch, wl.n_cand, 1024,
                       wl.prefill_chunk, "bf16", "greedy")
@@ -36,7 +36,8 @@ def _vp(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
-@pytest.mark.parametrize("M,N,K", [(13, 1024, 1024), (52, 3072, 1024), (208, 512, 1024), (7, 512, 1024), (300, 128, 64)])
+@pytest.mark.parametrize("M,N,K", [(13, 1024, 1024), (52, 3072, 1024), (208, 512, 1024), (7, 512, 1024),
+                                   (300, 128, 64), (13, 512, 4096), (52, 512, 4096)])
 @pytest.mark.parametrize("accumulate", [0, 1])
 def test_noalloc_matches_workspace_projection(ver, M, N, K, accumulate):
     lib = ver.lib
@@ -57,7 +58,7 @@ def test_noalloc_matches_workspace_projection(ver, M, N, K, accumulate):
 
 
 def test_noalloc_rejects_scratch_overflow(ver):
-    M, N, K = 512, 3072, 1024                # 6 splits x 512 x 3072 floats > 2^21
+    M, N, K = 512, 512, 4096                 # 32 splits x 512 x 512 partial floats > 2^21
     X = torch.zeros(M, K, device="cuda", dtype=torch.bfloat16)
     W = torch.zeros(N, K, device="cuda", dtype=torch.bfloat16)
     Y = torch.zeros(M, N, device="cuda")
