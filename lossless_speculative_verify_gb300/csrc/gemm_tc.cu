@@ -14,6 +14,8 @@
 // their 32 TMEM lanes for the epilogue.
 #include <cudaTypedefs.h>
 
+#include <type_traits>
+
 #include "evs_common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -27,6 +29,12 @@ constexpr int TC_A_BYTES = TC_BM * TC_BK * 2; // 16 KiB
 #endif
 #ifndef EVS_TC_CTA_TARGET
 #define EVS_TC_CTA_TARGET 304  // CTAs one projection aims to fill (two per SM)
+#endif
+#ifndef EVS_TC_WIDE_NARROW
+#define EVS_TC_WIDE_NARROW 0  // narrow outputs split beyond one cluster on the global path
+#endif
+#ifndef EVS_TC_DSMEM_BATCH
+#define EVS_TC_DSMEM_BATCH 8  // token rows whose peer loads the cluster reduction keeps in flight
 #endif
 #ifndef EVS_TC_MAX_SPLITS
 #define EVS_TC_MAX_SPLITS 8
@@ -255,23 +263,32 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             cluster_sync();
             const int lo = c_lo + (int)((long long)cnt * r / p.splits);
             const int hi = c_lo + (int)((long long)cnt * (r + 1) / p.splits);
-            for (int m = lo; m < hi; m += 8) {   // eight rows' peer loads in flight at once
-                float acc[8];
+            // RB rows' peer loads in flight at once; batching pays only with many rows
+            auto reduce_rows = [&](auto rb_tag) {
+                constexpr int RB = decltype(rb_tag)::value;
+                for (int m = lo; m < hi; m += RB) {
+                    float acc[RB];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) acc[u] = 0.f;
-                for (int sp = 0; sp < p.splits; ++sp) {
-                    const uint32_t peer = map_peer(base, (uint32_t)sp);
-                    float v[8];
+                    for (int u = 0; u < RB; ++u) acc[u] = 0.f;
+                    for (int sp = 0; sp < p.splits; ++sp) {
+                        const uint32_t peer = map_peer(base, (uint32_t)sp);
+                        float v[RB];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        v[u] = (m + u < hi) ? ld_peer_f32(peer + (uint32_t)((m + u - c_lo) * TC_BM + ch) * 4u) : 0.f;
+                        for (int u = 0; u < RB; ++u)
+                            v[u] = (m + u < hi) ? ld_peer_f32(peer + (uint32_t)((m + u - c_lo) * TC_BM + ch) * 4u)
+                                                : 0.f;
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) acc[u] += v[u];
+                        for (int u = 0; u < RB; ++u) acc[u] += v[u];
+                    }
+#pragma unroll
+                    for (int u = 0; u < RB; ++u)
+                        if (m + u < hi) finish(m + u, ch, acc[u], !bad);
                 }
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (m + u < hi) finish(m + u, ch, acc[u], !bad);
-            }
+            };
+            if (hi - lo >= 16)
+                reduce_rows(std::integral_constant<int, EVS_TC_DSMEM_BATCH>{});
+            else
+                reduce_rows(std::integral_constant<int, 1>{});
             cluster_sync();                       // peers finished reading this chunk
         }
     } else {
@@ -390,7 +407,7 @@ int tc_splits(int N, int K) {
     if (s > kblocks / EVS_TC_MIN_KB) s = kblocks / EVS_TC_MIN_KB;
     // stay within one portable cluster unless that leaves most SMs idle (narrow outputs such
     // as the LM head), where the global partial-sum path splits further
-    if (s > EVS_TC_MAX_SPLITS && tiles * EVS_TC_MAX_SPLITS >= 152) s = EVS_TC_MAX_SPLITS;
+    if (s > EVS_TC_MAX_SPLITS && (tiles * EVS_TC_MAX_SPLITS >= 152 || !EVS_TC_WIDE_NARROW)) s = EVS_TC_MAX_SPLITS;
     if (s < 1) s = 1;
     return s;
 }
