@@ -9,8 +9,9 @@
 // The CTA writes unnormalised partials (o, m, l) per query; the combine kernel merges the
 // chunks with the in-block causal keys.
 //
-// Warps 0-3 stage Q, run the softmax and the epilogue (warp w reads TMEM lanes 32w..32w+31),
-// warp 4 drives TMA, warp 5 issues the MMAs. dh = 128.
+// Warps 0-7 stage Q, run the softmax and the epilogue (warp w reads TMEM lanes
+// 32(w%4)..32(w%4)+31; the two warpgroups share the query columns), warp 8 drives TMA,
+// warp 9 issues the MMAs. dh = 128.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -40,7 +41,7 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int col_elem) {
     return (uint32_t)row * 128u + ((uint32_t)((col_elem >> 3) ^ (row & 7)) << 4) + (uint32_t)(col_elem & 7) * 2u;
 }
 
-__global__ void __launch_bounds__(192, 2)
+__global__ void __launch_bounds__(320, 2)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t tmem_slot[1];
@@ -84,18 +85,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             mbar_init(&empty[s], 1);
         }
         mbar_init(s_done, 1);
-        mbar_init(p_ready, 128);
+        mbar_init(p_ready, 256);
         mbar_init(o_done, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 4) {
+    if (warp == 8) {
         tmem_alloc(tmem_slot, (uint32_t)a.ncols);
         tmem_relinquish();
     }
-    if (tid < 128) {  // stage Q (fp32 -> bf16, swizzled K-major), zero rows past Q
+    if (tid < 256) {  // stage Q (fp32 -> bf16, swizzled K-major), zero rows past Q
         const float* qsrc = a.y + (size_t)b * a.Q * a.ldy + (size_t)head * AT_DH;
-        for (int e = tid; e < a.n_q * AT_DH; e += 128) {
+        for (int e = tid; e < a.n_q * AT_DH; e += 256) {
             const int q = e / AT_DH, c = e % AT_DH;
             const float v = q < a.Q ? qsrc[(size_t)q * a.ldy + c] : 0.f;
             *reinterpret_cast<__nv_bfloat16*>(sQ + (size_t)(c >> 6) * a.n_q * 128 + sw128_offset(q, c & 63)) =
@@ -109,7 +110,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     const uint32_t tmem = *tmem_slot;
     const uint32_t o_col = (uint32_t)(a.tiles * a.n_q);
 
-    if (warp == 4) {
+    if (warp == 8) {
         if (lane == 0) {  // ---- TMA: K tiles, then V tiles ---------------------------------
             const uint64_t pol = policy_evict_first();
             for (int i = 0; i < 2 * ntiles; ++i) {
@@ -125,7 +126,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             }
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         if (lane == 0) {  // ---- MMA issuer ----------------------------------------------------
             const uint32_t id_s = idesc_bf16_f32(AT_KEYS, a.n_q);
             const uint32_t id_o = idesc_bf16_f32_amn(AT_DH, a.n_q);
@@ -169,11 +170,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         __syncwarp();
     } else {
         // ---- softmax over the chunk: lane = key within a tile, columns = queries --------------
+        // Eight warps: warp w reads TMEM lanes 32(w%4).., warpgroup w/4 takes half of the
+        // 16-column query blocks. Scores go through exp2 with scale*log2(e) folded in.
+        const int grp = warp >> 2, wq = warp & 3;
+        const int nb = a.n_q / 16;
+        const int split_b = nb >= 2 ? (nb + 1) / 2 : nb;
+        const int g_lo = grp == 0 ? 0 : split_b * 16, g_hi = grp == 0 ? split_b * 16 : nb * 16;
+        const float sl = a.scale * 1.4426950408889634f;
         const bool sok = mbar_wait(s_done, 0);
         tc_fence_after();
-        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-        const int row = warp * 32 + lane;
-        for (int g = 0; g < a.n_q; g += 16) {
+        const uint32_t trow = tmem + ((uint32_t)(wq * 32) << 16);
+        const int row = wq * 32 + lane;
+        for (int g = g_lo; g < g_hi; g += 16) {
             float mx[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) mx[j] = -INFINITY;
@@ -182,20 +190,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 tmem_ld16(trow + (uint32_t)(t * a.n_q + g), v);
                 if (k_lo + t * AT_KEYS + row < k_hi) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) mx[j] = fmaxf(mx[j], v[j] * a.scale);
+                    for (int j = 0; j < 16; ++j) mx[j] = fmaxf(mx[j], v[j]);
                 }
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const float w = warp_max(mx[j]);
-                if (lane == j) red[warp][g + j] = w;
+                if (lane == j) red[wq][g + j] = w;
             }
         }
-        named_bar_sync(1, 128);
-        for (int q = tid; q < a.n_q; q += 128)
-            m_sh[q] = fmaxf(fmaxf(red[0][q], red[1][q]), fmaxf(red[2][q], red[3][q]));
-        named_bar_sync(1, 128);
-        for (int g = 0; g < a.n_q; g += 16) {
+        named_bar_sync(1, 256);
+        for (int q = tid; q < a.n_q; q += 256)   // raw-score max; scale > 0 keeps the order
+            m_sh[q] = fmaxf(fmaxf(red[0][q], red[1][q]), fmaxf(red[2][q], red[3][q])) * sl;
+        named_bar_sync(1, 256);
+        for (int g = g_lo; g < g_hi; g += 16) {
             float sum[16], mq[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) { sum[j] = 0.f; mq[j] = m_sh[g + j]; }
@@ -206,7 +214,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 uint8_t* pt = sP + (size_t)t * 2 * a.n_q * 128 + (size_t)(row >> 6) * a.n_q * 128;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float p = valid ? __expf(v[j] * a.scale - mq[j]) : 0.f;
+                    const float p = valid ? ex2_approx(fmaf(v[j], sl, -mq[j])) : 0.f;
                     const __nv_bfloat16 pb = __float2bfloat16_rn(p);
                     sum[j] += __bfloat162float(pb);   // normalise by what the MMA multiplies
                     *reinterpret_cast<__nv_bfloat16*>(pt + sw128_offset(g + j, row & 63)) = pb;
@@ -215,21 +223,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const float w = warp_sum(sum[j]);
-                if (lane == j) red[warp][g + j] = w;
+                if (lane == j) red[wq][g + j] = w;
             }
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        named_bar_sync(1, 128);
-        for (int q = tid; q < a.n_q; q += 128) l_sh[q] = red[0][q] + red[1][q] + red[2][q] + red[3][q];
+        named_bar_sync(1, 256);
+        for (int q = tid; q < a.n_q; q += 256) l_sh[q] = red[0][q] + red[1][q] + red[2][q] + red[3][q];
         mbar_arrive(p_ready);
         // ---- epilogue: lane = dh index, columns = queries --------------------------------------
         const bool ook = mbar_wait(o_done, 0);
         tc_fence_after();
         const bool bad = !sok || !ook || *abort_flag;
         if (bad && tid == 0) atomicOr(a.flags, (uint32_t)EVS_FLAG_TIMEOUT);
-        named_bar_sync(1, 128);
-        for (int g = 0; g < a.n_q; g += 16) {
+        named_bar_sync(1, 256);
+        for (int g = g_lo; g < g_hi; g += 16) {
             float v[16];
             tmem_ld16(trow + o_col + (uint32_t)g, v);
 #pragma unroll
@@ -238,14 +246,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 if (q < a.Q && !bad) part[(size_t)q * (AT_DH + 2) + row] = v[j];
             }
         }
-        for (int q = tid; q < a.Q; q += 128) {
-            part[(size_t)q * (AT_DH + 2) + AT_DH] = bad ? -INFINITY : m_sh[q];
+        // m in natural units of the scaled score (the combine's convention)
+        for (int q = tid; q < a.Q; q += 256) {
+            part[(size_t)q * (AT_DH + 2) + AT_DH] = bad ? -INFINITY : m_sh[q] * 0.6931471805599453f;
             part[(size_t)q * (AT_DH + 2) + AT_DH + 1] = bad ? 0.f : l_sh[q];
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 4) {
+    if (warp == 8) {
         tc_fence_after();
         tmem_dealloc(tmem, (uint32_t)a.ncols);
     }
@@ -335,7 +344,7 @@ bool launch_attn_tc(evs_handle* h, int li, const Pass& p, const AttnPlan& plan) 
         return false;
     AttnArgs a{h->y, 3 * h->cfg.d, H, p.C * p.T, plan.n_q, plan.tiles, plan.splits, h->g.q_max, plan.stages,
                plan.ncols, 1.0f / sqrtf((float)AT_DH), h->kv_base, h->attn_part, h->flags};
-    return launch_k(h, attn_tc_kernel, dim3(plan.splits, p.B * H), dim3(192), (size_t)plan.smem, tk, tv, a) ==
+    return launch_k(h, attn_tc_kernel, dim3(plan.splits, p.B * H), dim3(320), (size_t)plan.smem, tk, tv, a) ==
            cudaSuccess;
 }
 
