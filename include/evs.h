@@ -253,7 +253,8 @@ evs_status evs_debug_projection(evs_handle* h, const void* X, int32_t x_rows, co
  * while they execute (plugin-style engines), and for latency-critical loops where an
  * allocation would synchronise the device.
  * Computes Y[m][n] (+)= sum_k X[m][k] W[n][k] with the same tcgen05 kernel as
- * evs_debug_projection. X: device bf16 [x_rows][K] (x_rows >= M); W: device bf16
+ * evs_debug_projection; split-K partial sums always go through the fixed array (never
+ * through a thread-block cluster). X: device bf16 [x_rows][K] (x_rows >= M); W: device bf16
  * out-major [N][K]; Y: device fp32 [M][ldy]; stream: a cudaStream_t. Needs M <= 512,
  * N % 128 == 0, N <= 32768, K % 64 == 0.
  * Scratch: one fixed array of 8 MiB of fp32 partial sums (plus 256 counters) compiled

@@ -561,7 +561,9 @@ extern "C" evs_status evs_projection_noalloc(const void* X, int32_t x_rows, cons
         g_noalloc_ptr[dev] = p;
     }
     NoAllocScratch* sc = g_noalloc_ptr[dev];
-    const TcShape t = tc_shape(M, N, K);
+    // split-K partials always go through the fixed array here (no thread-block cluster)
+    TcShape t = tc_shape(M, N, K);
+    t.cluster = 0;
     if (tc_part_floats(t, M, N) > kNoAllocPartFloats) return EVS_ERR_CAPACITY;
     CUtensorMap ta, tb;
     if (!make_map(&ta, W, (uint64_t)N, (uint64_t)K, TC_BM)) return EVS_ERR_CUDA;

@@ -58,7 +58,7 @@ def test_noalloc_matches_workspace_projection(ver, M, N, K, accumulate):
 
 
 def test_noalloc_rejects_scratch_overflow(ver):
-    M, N, K = 512, 512, 4096                 # 32 splits x 512 x 512 partial floats > 2^21
+    M, N, K = 512, 1024, 4096                # 8 splits x 512 x 1024 partial floats > 2^21
     X = torch.zeros(M, K, device="cuda", dtype=torch.bfloat16)
     W = torch.zeros(N, K, device="cuda", dtype=torch.bfloat16)
     Y = torch.zeros(M, N, device="cuda")
