@@ -42,6 +42,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-also", action="store_true", help="skip the secondary workloads")
     return ap.parse_args()
 
 
@@ -163,8 +164,40 @@ def oracle_rate(wl, seconds, rounds_from=0):
                       f"{dt:.1f} s", "us_per_round": dt / rounds * 1e6}
 
 
+# ------------------------------------------------------------------------------- ranks
+def aggregate(ms, e2e_ms, tokens, e2e_tokens, device):
+    """Whole-job figures over the ranks of the process group (if any): the slowest rank's
+    times, the sum of every rank's verified tokens."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms, e2e_ms, tokens, e2e_tokens
+    t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    c = torch.tensor([tokens, e2e_tokens], dtype=torch.int64, device=device)
+    dist.all_reduce(c)
+    return float(t[0]), float(t[1]), int(c[0]), int(c[1])
+
+
+def traffic_per_round(wl, kind):
+    """DRAM bytes one round's launches of a kernel kind moved in an ncu capture, as recorded
+    in profiles/traffic.txt, if the kernel source is unchanged since (else None)."""
+    import hashlib
+    src = {"gemm": "gemm_tc.cu", "attn": "attn_tc.cu"}.get(kind)
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if src is None or not os.path.exists(path):
+        return None
+    digest = hashlib.sha256(open(os.path.join(ROOT, "lossless_speculative_verify_gb300", "csrc", src),
+                                 "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        f = line.split()
+        if len(f) == 4 and f[0] == wl.name and f[1] == kind and f[3] == digest:
+            return float(f[2])
+    return None
+
+
 # ------------------------------------------------------------------------------- GPU arm
-def run_evs(args, wl, rank, world):
+def run_evs(args, wl, rank, world, light=False):
     import torch
     from lossless_speculative_verify_gb300.build import build
     from lossless_speculative_verify_gb300 import DeviceWeights, Verifier, make_config
@@ -262,6 +295,8 @@ def run_evs(args, wl, rank, world):
     ms = sum(a.elapsed_time(b) for a, b in evs)
     tokens = int(tok_acc.sum().item())
     clk = clocks.stop() if clocks is not None else None
+    if light:
+        return dict(ms=ms, tokens=tokens, clocks=clk, flags=ver.flags(), graph=graph is not None)
     # end-to-end through the public API: pinned host inputs in, accepted length and
     # correction out, every step
     e2e_ms = 0.0
@@ -315,14 +350,7 @@ def run_evs(args, wl, rank, world):
         prof = ver.profile_read()
     ver.profile(False)
     flags = ver.flags()
-    # max over ranks
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
-        c = torch.tensor([tokens, e2e_tokens], dtype=torch.int64, device=dev)
-        torch.distributed.all_reduce(c)
-        tokens, e2e_tokens = int(c[0]), int(c[1])
+    ms, e2e_ms, tokens, e2e_tokens = aggregate(ms, e2e_ms, tokens, e2e_tokens, dev)
     return dict(ms=ms, tokens=tokens, e2e_ms=e2e_ms, e2e_tokens=e2e_tokens, h2d=h2d, d2h=d2h,
                 prof=prof, n_prof=n_prof, prof_mode=prof_mode, launches_round=launches_round, clocks=clk,
                 flags=flags, graph=graph is not None)
@@ -386,7 +414,8 @@ def main():
         rounds_prof = out["n_prof"]
         achieved = dom_bytes * rounds_prof / (prof[dom][1] / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "traffic": None, "peak_source": pk_kind,
+                "frac": achieved / pk["hbm_gbs"], "traffic": traffic_per_round(wl, dom),
+                "algorithmic_bytes_per_round": dom_bytes, "peak_source": pk_kind,
                 "share_of_round": prof[dom][1] / sum(v[1] for v in prof.values()),
                 "timing": f"event pairs around each launch, {out['prof_mode']} replay of {out['n_prof']} rounds"}
     line = {
@@ -409,6 +438,25 @@ def main():
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_rate(wl, args.cpu_seconds)
+    if world == 1 and not args.no_also:
+        # the other bf16 workloads, measured the same way with fewer steps (context for the
+        # roofline targets on the 4096-wide and long-context shapes)
+        also = {}
+        for name in ("d4096_l32_p8k_bf16", "d4096_l4_p256k_bf16", "d4096_l8_p32k_b4c4_bf16"):
+            if name == wl.name:
+                continue
+            w2 = get_workload(name)
+            sub = argparse.Namespace(**vars(args))
+            sub.steps, sub.warmup = max(5, K // 4), 3
+            o2 = run_evs(sub, w2, rank, world, light=True)
+            r_s = o2["ms"] / sub.steps / 1e3
+            b2 = round_bytes_min(w2, w2.prefix_len + sub.warmup + sub.steps)
+            also[name] = {"us_per_round": round(r_s * 1e6, 2), "value": o2["tokens"] / (o2["ms"] / 1e3),
+                          "unit": UNIT, "steps": sub.steps, "bytes_min": b2,
+                          "round_roofline_frac": round(b2 / (pk["hbm_gbs"] * 1e9) / r_s, 4),
+                          "clocks": o2["clocks"], "device_flags": o2["flags"]}
+            torch.cuda.empty_cache()
+        line["also"] = also
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
