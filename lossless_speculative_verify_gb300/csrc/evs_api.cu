@@ -270,24 +270,30 @@ void run_layers(evs_handle* h, const int32_t* tokens, int tok_stride, const int3
     if (h->fused) {
         // RMS norm folded into the projections: consumers of h read bf16(h) and scale their
         // output rows by 1/rms(h); producers of h leave bf16(h) and per-tile sums of squares
-        const evs::GemmFuse in{h->ssq, d / 128, h->g.M_max, d, nullptr, 0, nullptr};
-        const evs::GemmFuse out{nullptr, 0, h->g.M_max, d, h->hb, d, h->ssq};
+        const evs::GemmFuse in{h->ssq, d / 128, h->g.M_max, d, nullptr, 0, nullptr, -1, -1, &p};
+        const evs::GemmFuse out{nullptr, 0, h->g.M_max, d, h->hb, d, h->ssq, -1, -1, &p};
         for (int li = 0; li < c.n_layers; ++li) {
             const evs_layer_weights& W = h->w.layer[li];
+            int fused = 0;
+            evs::GemmFuse mixin = in;
             switch (c.layer_kind[li]) {
                 case EVS_LAYER_FIR:
-                    evs::launch_gemm(h, h->hb, W.w_in, h->y, p.M, d, d, 3 * d, 0, &in);
-                    evs::launch_fir(h, li, p);
-                    evs::launch_gemm(h, h->act, W.w_out, h->h, p.M, d, d, d, 1, &out);
-                    break;
                 case EVS_LAYER_IIR:
-                    evs::launch_gemm(h, h->hb, W.w_in, h->y, p.M, d, d, 3 * d, 0, &in);
-                    evs::launch_iir(h, li, p);
+                    // the mixer runs in the in-projection's epilogue when the shape allows
+                    mixin.mix_layer = h->fuse_mixer ? li : -1;
+                    evs::launch_gemm(h, h->hb, W.w_in, h->y, p.M, d, d, 3 * d, 0, &mixin, &fused);
+                    if (!(fused & 1)) {
+                        if (c.layer_kind[li] == EVS_LAYER_FIR)
+                            evs::launch_fir(h, li, p);
+                        else
+                            evs::launch_iir(h, li, p);
+                    }
                     evs::launch_gemm(h, h->act, W.w_out, h->h, p.M, d, d, d, 1, &out);
                     break;
                 default:
-                    evs::launch_gemm(h, h->hb, W.w_qkv, h->y, p.M, 3 * d, d, 3 * d, 0, &in);
-                    evs::launch_kv_write(h, li, p);
+                    mixin.kv_layer = li;   // K/V rows written straight from the QKV epilogue
+                    evs::launch_gemm(h, h->hb, W.w_qkv, h->y, p.M, 3 * d, d, 3 * d, 0, &mixin, &fused);
+                    if (!(fused & 2)) evs::launch_kv_write(h, li, p);
                     evs::launch_attention(h, li, p);
                     evs::launch_gemm(h, h->act, W.w_o, h->h, p.M, d, d, d, 1, &out);
             }
@@ -349,6 +355,7 @@ evs_status evs_create(const evs_config* cfg, const evs_weights* weights, void* w
     carve(*cfg, h->ws, h);
     h->tc_smem_max = 0;
     h->pdl = 1;
+    h->fuse_mixer = 1;
     // the norm is folded into the tensor-core projections when every projection shape runs
     // on them (bf16, widths in whole 128-channel tiles)
     h->fused = cfg->dtype == EVS_DTYPE_BF16 && cfg->d % 128 == 0 && cfg->vocab % 128 == 0 && h->g.M_max <= 512;

@@ -45,12 +45,16 @@ struct AttnPlan {
 };
 
 // Fused-norm extras of one projection (null members are unused).
+struct Pass;
 struct GemmFuse {
     const float* ssq_in;     // rows scaled by 1/rms from these per-tile sums of squares
     int ssq_tiles, ssq_ld, norm_d;
     __nv_bfloat16* hb_out;   // bf16 copy of the final values
     int hb_ld;
     float* ssq_out;          // per-tile sums of squares of the final values
+    int mix_layer;           // >= 0: run this FIR / IIR layer's mixer in the epilogue if it fits
+    int kv_layer;            // >= 0: write this attention layer's K/V from the epilogue
+    const Pass* pass;        // the pass shape (needed by the two above)
 };
 
 // A pass runs B sequences x C candidates x T block positions; row m = (b*C + c)*T + i.
@@ -101,6 +105,7 @@ struct evs_handle {
     int verified;         // a verify was enqueued since the last slice / prefill
     int launches;         // kernels enqueued by the last public call
     int pdl;              // launch with programmatic dependent launch
+    int fuse_mixer;       // run FIR / IIR mixers in the in-projection epilogue when they fit
     void* prof;           // evs::Profiler*, lazily created
     int prof_on;
 };
@@ -115,8 +120,9 @@ void prof_end(evs_handle* h, int kind);
 void launch_embed(evs_handle* h, const int32_t* tokens, int tok_stride_bc, const int32_t* anchor,
                   const Pass& p);
 void launch_rmsnorm(evs_handle* h, const Pass& p);
+// fused (if non-null) returns bit 0: the mixer ran in the epilogue, bit 1: K/V were written
 void launch_gemm(evs_handle* h, const void* A, const void* W, float* Y, int M, int N, int K,
-                 int ldy, int accumulate, const GemmFuse* fz = nullptr);
+                 int ldy, int accumulate, const GemmFuse* fz = nullptr, int* fused = nullptr);
 // tcgen05 projection (gemm_tc.cu); false when it cannot take the shape
 bool gemm_tc_supported(int M, int N, int K);
 int gemm_tc_init();
@@ -126,7 +132,7 @@ AttnPlan attn_tc_plan(int Q, int B, int H, int t_max, int smem_max);
 int attn_tc_init();
 bool launch_attn_tc(evs_handle* h, int layer, const Pass& p, const AttnPlan& plan);
 bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, float* Y, int M, int N,
-                    int K, int ldy, int accumulate, const GemmFuse* fz = nullptr);
+                    int K, int ldy, int accumulate, const GemmFuse* fz = nullptr, int* fused = nullptr);
 void launch_fir(evs_handle* h, int layer, const Pass& p);
 void launch_iir(evs_handle* h, int layer, const Pass& p);
 void launch_kv_write(evs_handle* h, int layer, const Pass& p);

@@ -68,6 +68,26 @@ struct TcArgs {
     __nv_bfloat16* hb_out; // [M][hb_ld] or null
     int hb_ld;
     float* ssq_out;        // [N / 128][ssq_ld] or null
+    // fused mixer of a FIR / IIR layer's in-projection (0 none, 1 FIR, 2 IIR): the product
+    // v (or u) never reaches global memory; the mixer output goes to mix_out in bf16
+    int mix, mix_C, mix_T, mix_commit, mix_param, d;   // param: FIR taps L or IIR poles N
+    __nv_bfloat16* mix_out;                            // [M][d]
+    const float* taps;
+    float* tail;
+    float* stage;
+    const float2* lam;
+    const float2* bq;
+    const float2* cq;
+    float2* state;
+    float2* ret;
+    // fused K/V write of an attention layer's QKV projection: columns [d, 3d) go to the
+    // cache (one candidate) or the per-candidate side buffer instead of Y
+    int kv, kv_H, kv_dh, kv_in_cache, kv_tmax, kv_C, kv_T;
+    const int32_t* kv_base;
+    __nv_bfloat16* kc;
+    __nv_bfloat16* vc;
+    __nv_bfloat16* ks;
+    __nv_bfloat16* vs;
 };
 
 __global__ void __launch_bounds__(128, 2)
@@ -220,6 +240,25 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     auto finish = [&](int m, int nl, float v, bool live) {
         if (p.ssq_in) v *= rinv_s[m];
         float out = v;
+        if (p.kv && n0 + nl >= p.d) {
+            if (live) {
+                const int c2 = n0 + nl - p.d, which = c2 / p.d, col = c2 % p.d;
+                const int hh = col / p.kv_dh, e = col % p.kv_dh;
+                const int bc = m / p.kv_T, i = m % p.kv_T, b = bc / p.kv_C;
+                if (p.kv_in_cache) {
+                    const int t = p.kv_base[b] + i;
+                    if (t < p.kv_tmax)
+                        (which ? p.vc : p.kc)[(((size_t)b * p.kv_H + hh) * p.kv_tmax + t) * p.kv_dh + e] =
+                            __float2bfloat16_rn(out);
+                    else
+                        atomicOr(p.flags, (uint32_t)EVS_FLAG_KV_OVERFLOW);
+                } else {
+                    (which ? p.vs : p.ks)[(((size_t)bc * p.kv_H + hh) * p.kv_T + i) * p.kv_dh + e] =
+                        __float2bfloat16_rn(out);
+                }
+            }
+            return;
+        }
         if (live) {
             float* dst = p.Y + (size_t)m * p.ldy + n0 + nl;
             if (p.accumulate) out += *dst;
@@ -234,7 +273,95 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     int own_lo = 0, own_hi = 0;   // token rows whose sums of squares this CTA completes
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
     const int nl_lane = warp * 32 + lane;
-    if (p.splits == 1) {
+    if (p.mix) {
+        // ---- in-projection + mixer: gather this CTA's channel slice of v for every token
+        // row (whole tile without split-K; a 1/S share of the channels with a cluster), then
+        // one thread per (sequence-candidate, channel) runs the FIR / modal IIR over time
+        float* park = reinterpret_cast<float*>(smem);            // [M][128] this CTA's partials
+        const int S = p.splits;
+        const int c_lo = (int)(128LL * split / S), c_hi = (int)(128LL * (split + 1) / S);
+        const int cw = c_hi - c_lo;
+        float* vals = S == 1 ? park : park + (size_t)p.M * TC_BM;   // [M][cw] final values
+        for (int c0 = 0; c0 < p.M; c0 += 16) {
+            float v[16];
+            tmem_ld16(trow + (uint32_t)c0, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (c0 + j < p.M) park[(size_t)(c0 + j) * TC_BM + nl_lane] = v[j];
+        }
+        if (S > 1) {
+            cluster_sync();
+            const uint32_t base = smem_u32(park);
+            for (int idx = threadIdx.x; idx < p.M * cw; idx += blockDim.x) {
+                const int m = idx / cw, c = idx % cw;
+                float acc = 0.f;
+                for (int sp = 0; sp < S; ++sp)
+                    acc += ld_peer_f32(map_peer(base + (uint32_t)(m * TC_BM + c_lo + c) * 4u, (uint32_t)sp));
+                vals[idx] = acc;
+            }
+            cluster_sync();                       // peers finished reading this CTA's park
+        }
+        __syncthreads();
+        const int vld = S == 1 ? TC_BM : cw;      // row stride of vals
+        const int T = p.mix_T, groups = p.M / T;
+        for (int pair = threadIdx.x; pair < groups * cw && !bad; pair += blockDim.x) {
+            const int g = pair / cw, c = pair % cw, n = n0 + c_lo + c, b = g / p.mix_C;
+            const float* vrow = vals + (size_t)g * T * vld + (S == 1 ? c_lo + c : c);
+            if (p.mix == 1) {
+                const int L = p.mix_param;
+                float w[16], hist[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    w[j] = (j < L) ? p.taps[(size_t)n * L + j] : 0.f;
+                    hist[j] = (j < L - 1) ? p.tail[((size_t)b * (L - 1) + j) * p.d + n] : 0.f;
+                }
+                float* st = p.stage + (size_t)g * (L - 1 + T) * p.d;
+                if (!p.mix_commit)
+                    for (int j = 0; j < L - 1; ++j) st[(size_t)j * p.d + n] = hist[j];
+                for (int t = 0; t < T; ++t) {
+                    const float v = vrow[(size_t)t * vld] * (p.ssq_in ? rinv_s[g * T + t] : 1.f);
+                    float y = w[0] * v;
+#pragma unroll
+                    for (int j = 1; j < 16; ++j)
+                        if (j < L) y = fmaf(w[j], hist[L - 1 - j], y);
+#pragma unroll
+                    for (int j = 0; j < 15; ++j)
+                        if (j < L - 2) hist[j] = hist[j + 1];
+                    hist[L - 2] = v;
+                    p.mix_out[((size_t)g * T + t) * p.d + n] = __float2bfloat16_rn(y);
+                    if (!p.mix_commit) st[(size_t)(L - 1 + t) * p.d + n] = v;
+                }
+                if (p.mix_commit)
+                    for (int j = 0; j < L - 1; ++j) p.tail[((size_t)b * (L - 1) + j) * p.d + n] = hist[j];
+            } else {
+                const int N = p.mix_param;            // <= 16 on this path
+                float2 sv[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    sv[k] = (k < N) ? p.state[((size_t)b * p.d + n) * N + k] : make_float2(0.f, 0.f);
+                for (int t = 0; t < T; ++t) {
+                    const float u = vrow[(size_t)t * vld] * (p.ssq_in ? rinv_s[g * T + t] : 1.f);
+                    float y = 0.f;
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        if (k >= N) break;
+                        const float2 l = p.lam[(size_t)n * N + k], bq = p.bq[(size_t)n * N + k],
+                                     cq = p.cq[(size_t)n * N + k];
+                        const float sx = fmaf(l.x, sv[k].x, fmaf(-l.y, sv[k].y, bq.x * u));
+                        const float sy = fmaf(l.x, sv[k].y, fmaf(l.y, sv[k].x, bq.y * u));
+                        sv[k] = make_float2(sx, sy);
+                        y = fmaf(cq.x, sx, fmaf(-cq.y, sy, y));
+                        if (!p.mix_commit) p.ret[(((size_t)g * T + t) * p.d + n) * N + k] = sv[k];
+                    }
+                    p.mix_out[((size_t)g * T + t) * p.d + n] = __float2bfloat16_rn(y);
+                }
+                if (p.mix_commit)
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        if (k < N) p.state[((size_t)b * p.d + n) * N + k] = sv[k];
+            }
+        }
+    } else if (p.splits == 1) {
         for (int c0 = 0; c0 < p.M; c0 += 16) {
             float v[16];
             tmem_ld16(trow + (uint32_t)c0, v);
@@ -489,7 +616,8 @@ bool gemm_tc_supported(int M, int N, int K) {
 
 // Returns false (nothing launched) if a tensor map could not be built.
 bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, float* Y, int M, int N, int K,
-                    int ldy, int accumulate, const GemmFuse* fz) {
+                    int ldy, int accumulate, const GemmFuse* fz, int* fused) {
+    if (fused) *fused = 0;
     const TcShape t = tc_shape(M, N, K, h->gemm_part_floats);
     CUtensorMap ta, tb;
 #if EVS_TC_PACKED
@@ -499,8 +627,12 @@ bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, flo
 #endif
     if (!make_map(&tb, X, (uint64_t)x_rows, (uint64_t)K, (uint32_t)(t.n_pad < 256 ? t.n_pad : 256))) return false;
     if ((int)t.smem > h->tc_smem_max) return false;
-    TcArgs a{Y, ldy, M, N, t.kblocks, t.splits, t.n_pad, t.stages, accumulate, t.ncols, t.kbs, t.cluster,
-             t.park_rows, h->gemm_part, h->gemm_counters, h->flags, nullptr, 0, 0, 0, nullptr, 0, nullptr};
+    TcArgs a{};
+    a.Y = Y; a.ldy = ldy; a.M = M; a.N = N; a.kblocks = t.kblocks; a.splits = t.splits; a.n_pad = t.n_pad;
+    a.stages = t.stages; a.accumulate = accumulate; a.ncols = t.ncols; a.kbs = t.kbs; a.cluster = t.cluster;
+    a.park_rows = t.park_rows; a.part = h->gemm_part; a.counters = h->gemm_counters; a.flags = h->flags;
+    a.d = h->cfg.d;
+    int did = 0;
     if (fz) {
         a.ssq_in = fz->ssq_in;
         a.ssq_tiles = fz->ssq_tiles;
@@ -509,8 +641,55 @@ bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, flo
         a.hb_out = fz->hb_out;
         a.hb_ld = fz->hb_ld;
         a.ssq_out = fz->ssq_out;
+        const Pass* ps = fz->pass;
+        const size_t ring = (size_t)t.stages * t.kbs * (TC_A_BYTES + t.n_pad * 128);
+        if (fz->mix_layer >= 0 && ps) {
+            // the mixer runs in the epilogue when the whole partial tile (plus the reduced
+            // channel slice) sits in the ring at once and the split is a cluster or none
+            const LayerDesc& L = h->layer[fz->mix_layer];
+            const evs_layer_weights& LW = h->w.layer[fz->mix_layer];
+            const int cw = (TC_BM + t.splits - 1) / t.splits;
+            const size_t need = (size_t)M * TC_BM * 4 + (t.splits > 1 ? (size_t)M * cw * 4 : 0);
+            const bool shape_ok = (t.splits == 1 || t.cluster) && need <= ring && M % ps->T == 0 &&
+                                  (L.kind == EVS_LAYER_FIR || L.param <= 16);
+            if (shape_ok) {
+                a.mix = L.kind == EVS_LAYER_FIR ? 1 : 2;
+                a.mix_C = ps->C;
+                a.mix_T = ps->T;
+                a.mix_commit = ps->commit;
+                a.mix_param = L.param;
+                a.mix_out = (__nv_bfloat16*)h->act;
+                a.taps = LW.fir_taps;
+                a.tail = L.tail;
+                a.stage = L.stage;
+                a.lam = (const float2*)LW.iir_lambda;
+                a.bq = (const float2*)LW.iir_b;
+                a.cq = (const float2*)LW.iir_c;
+                a.state = L.state;
+                a.ret = L.ret;
+                did |= 1;
+            }
+        }
+        if (fz->kv_layer >= 0 && ps) {
+            const LayerDesc& L = h->layer[fz->kv_layer];
+            a.kv = 1;
+            a.kv_H = L.param;
+            a.kv_dh = h->cfg.head_dim;
+            a.kv_in_cache = ps->kv_in_cache;
+            a.kv_tmax = h->cfg.t_max;
+            a.kv_C = ps->C;
+            a.kv_T = ps->T;
+            a.kv_base = h->kv_base;
+            a.kc = (__nv_bfloat16*)L.kc;
+            a.vc = (__nv_bfloat16*)L.vc;
+            a.ks = (__nv_bfloat16*)L.ks;
+            a.vs = (__nv_bfloat16*)L.vs;
+            did |= 2;
+        }
     }
-    return launch_tc(t, ta, tb, a, h->stream, h->pdl != 0);
+    if (!launch_tc(t, ta, tb, a, h->stream, h->pdl != 0)) return false;
+    if (fused) *fused = did;
+    return true;
 }
 
 }  // namespace evs
@@ -572,8 +751,10 @@ extern "C" evs_status evs_projection_noalloc(const void* X, int32_t x_rows, cons
     cudaStream_t s = (cudaStream_t)stream;
     // the array keeps the previous call's contents: the counters must start at zero
     if (cudaMemsetAsync(sc->counters, 0, sizeof(sc->counters), s) != cudaSuccess) return EVS_ERR_CUDA;
-    TcArgs a{Y, ldy, M, N, t.kblocks, t.splits, t.n_pad, t.stages, accumulate, t.ncols, t.kbs, t.cluster,
-             t.park_rows, sc->part, sc->counters, &sc->flags, nullptr, 0, 0, 0, nullptr, 0, nullptr};
+    TcArgs a{};
+    a.Y = Y; a.ldy = ldy; a.M = M; a.N = N; a.kblocks = t.kblocks; a.splits = t.splits; a.n_pad = t.n_pad;
+    a.stages = t.stages; a.accumulate = accumulate; a.ncols = t.ncols; a.kbs = t.kbs; a.cluster = t.cluster;
+    a.park_rows = t.park_rows; a.part = sc->part; a.counters = sc->counters; a.flags = &sc->flags;
     if (!launch_tc(t, ta, tb, a, s, false)) return EVS_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? EVS_OK : EVS_ERR_CUDA;
 }

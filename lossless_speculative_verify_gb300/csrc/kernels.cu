@@ -754,10 +754,11 @@ void launch_rmsnorm(evs_handle* h, const Pass& p) {
 }
 
 void launch_gemm(evs_handle* h, const void* A, const void* W, float* Y, int M, int N, int K, int ldy,
-                 int accumulate, const GemmFuse* fz) {
+                 int accumulate, const GemmFuse* fz, int* fused) {
     prof_begin(h, EVS_K_GEMM);
+    if (fused) *fused = 0;
     if (is_bf16(h) && gemm_tc_supported(M, N, K) &&
-        launch_gemm_tc(h, A, h->g.M_max, W, Y, M, N, K, ldy, accumulate, fz)) {
+        launch_gemm_tc(h, A, h->g.M_max, W, Y, M, N, K, ldy, accumulate, fz, fused)) {
         h->launches++;
         prof_end(h, EVS_K_GEMM);
         return;
