@@ -304,10 +304,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         __syncthreads();
         const int vld = S == 1 ? TC_BM : cw;      // row stride of vals
         const int T = p.mix_T, groups = p.M / T;
-        for (int pair = threadIdx.x; pair < groups * cw && !bad; pair += blockDim.x) {
-            const int g = pair / cw, c = pair % cw, n = n0 + c_lo + c, b = g / p.mix_C;
-            const float* vrow = vals + (size_t)g * T * vld + (S == 1 ? c_lo + c : c);
-            if (p.mix == 1) {
+        const int voff = S == 1 ? c_lo : 0;       // column of this CTA's first channel in vals
+        if (p.mix == 1 && !bad) {
+            // FIR: one thread per (sequence-candidate, channel)
+            for (int pair = threadIdx.x; pair < groups * cw; pair += blockDim.x) {
+                const int g = pair / cw, c = pair % cw, n = n0 + c_lo + c, b = g / p.mix_C;
+                const float* vrow = vals + (size_t)g * T * vld + voff + c;
                 const int L = p.mix_param;
                 float w[16], hist[16];
 #pragma unroll
@@ -333,32 +335,38 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
                 if (p.mix_commit)
                     for (int j = 0; j < L - 1; ++j) p.tail[((size_t)b * (L - 1) + j) * p.d + n] = hist[j];
-            } else {
-                const int N = p.mix_param;            // <= 16 on this path
-                float2 sv[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    sv[k] = (k < N) ? p.state[((size_t)b * p.d + n) * N + k] : make_float2(0.f, 0.f);
-                for (int t = 0; t < T; ++t) {
-                    const float u = vrow[(size_t)t * vld] * (p.ssq_in ? rinv_s[g * T + t] : 1.f);
-                    float y = 0.f;
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        if (k >= N) break;
-                        const float2 l = p.lam[(size_t)n * N + k], bq = p.bq[(size_t)n * N + k],
-                                     cq = p.cq[(size_t)n * N + k];
-                        const float sx = fmaf(l.x, sv[k].x, fmaf(-l.y, sv[k].y, bq.x * u));
-                        const float sy = fmaf(l.x, sv[k].y, fmaf(l.y, sv[k].x, bq.y * u));
-                        sv[k] = make_float2(sx, sy);
-                        y = fmaf(cq.x, sx, fmaf(-cq.y, sy, y));
-                        if (!p.mix_commit) p.ret[(((size_t)g * T + t) * p.d + n) * N + k] = sv[k];
-                    }
-                    p.mix_out[((size_t)g * T + t) * p.d + n] = __float2bfloat16_rn(y);
+            }
+        } else if (p.mix == 2) {
+            // modal IIR: N consecutive lanes hold the N poles of one channel (N divides 32),
+            // the readout summed by a shuffle reduction over them
+            const int N = p.mix_param;
+            const int items = groups * cw * N;                    // (group, channel, pole)
+            const int span = (items + 31) / 32 * 32;              // whole warps take part
+            for (int it = threadIdx.x; it < span; it += blockDim.x) {
+                const bool on = it < items && !bad;
+                const int k = it % N, c = (it / N) % cw, g = min(it / (N * cw), groups - 1);
+                const int n = n0 + c_lo + c, b = g / p.mix_C;
+                const float* vrow = vals + (size_t)g * T * vld + voff + c;
+                float2 l = make_float2(0.f, 0.f), bq = l, cq = l, sv = l;
+                if (on) {
+                    l = p.lam[(size_t)n * N + k];
+                    bq = p.bq[(size_t)n * N + k];
+                    cq = p.cq[(size_t)n * N + k];
+                    sv = p.state[((size_t)b * p.d + n) * N + k];
                 }
-                if (p.mix_commit)
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        if (k < N) p.state[((size_t)b * p.d + n) * N + k] = sv[k];
+                for (int t = 0; t < T; ++t) {
+                    const float u = on ? vrow[(size_t)t * vld] * (p.ssq_in ? rinv_s[g * T + t] : 1.f) : 0.f;
+                    const float sx = fmaf(l.x, sv.x, fmaf(-l.y, sv.y, bq.x * u));
+                    const float sy = fmaf(l.x, sv.y, fmaf(l.y, sv.x, bq.y * u));
+                    sv = make_float2(sx, sy);
+                    float part = fmaf(cq.x, sx, -cq.y * sy);
+                    for (int o = N >> 1; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                    if (on) {
+                        if (k == 0) p.mix_out[((size_t)g * T + t) * p.d + n] = __float2bfloat16_rn(part);
+                        if (!p.mix_commit) p.ret[(((size_t)g * T + t) * p.d + n) * N + k] = sv;
+                    }
+                }
+                if (on && p.mix_commit) p.state[((size_t)b * p.d + n) * N + k] = sv;
             }
         }
     } else if (p.splits == 1) {
@@ -651,7 +659,7 @@ bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, flo
             const int cw = (TC_BM + t.splits - 1) / t.splits;
             const size_t need = (size_t)M * TC_BM * 4 + (t.splits > 1 ? (size_t)M * cw * 4 : 0);
             const bool shape_ok = (t.splits == 1 || t.cluster) && need <= ring && M % ps->T == 0 &&
-                                  (L.kind == EVS_LAYER_FIR || L.param <= 16);
+                                  (L.kind == EVS_LAYER_FIR || 32 % L.param == 0);
             if (shape_ok) {
                 a.mix = L.kind == EVS_LAYER_FIR ? 1 : 2;
                 a.mix_C = ps->C;
