@@ -294,9 +294,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint32_t base = smem_u32(park);
             for (int idx = threadIdx.x; idx < p.M * cw; idx += blockDim.x) {
                 const int m = idx / cw, c = idx % cw;
+                const uint32_t off = base + (uint32_t)(m * TC_BM + c_lo + c) * 4u;
+                float v[8];   // every peer's value requested before any is added (S <= 8)
+#pragma unroll
+                for (int sp = 0; sp < 8; ++sp) v[sp] = sp < S ? ld_peer_f32(map_peer(off, (uint32_t)sp)) : 0.f;
                 float acc = 0.f;
-                for (int sp = 0; sp < S; ++sp)
-                    acc += ld_peer_f32(map_peer(base + (uint32_t)(m * TC_BM + c_lo + c) * 4u, (uint32_t)sp));
+#pragma unroll
+                for (int sp = 0; sp < 8; ++sp) acc += v[sp];
                 vals[idx] = acc;
             }
             cluster_sync();                       // peers finished reading this CTA's park
@@ -405,16 +409,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     float acc[RB];
 #pragma unroll
                     for (int u = 0; u < RB; ++u) acc[u] = 0.f;
-                    for (int sp = 0; sp < p.splits; ++sp) {
-                        const uint32_t peer = map_peer(base, (uint32_t)sp);
-                        float v[RB];
+                    // all peers' values for RB rows requested before any is added (splits <= 8)
+                    float v[8][RB];
+#pragma unroll
+                    for (int sp = 0; sp < 8; ++sp) {
+                        const uint32_t peer = map_peer(base, (uint32_t)(sp < p.splits ? sp : 0));
 #pragma unroll
                         for (int u = 0; u < RB; ++u)
-                            v[u] = (m + u < hi) ? ld_peer_f32(peer + (uint32_t)((m + u - c_lo) * TC_BM + ch) * 4u)
-                                                : 0.f;
-#pragma unroll
-                        for (int u = 0; u < RB; ++u) acc[u] += v[u];
+                            v[sp][u] = (sp < p.splits && m + u < hi)
+                                           ? ld_peer_f32(peer + (uint32_t)((m + u - c_lo) * TC_BM + ch) * 4u)
+                                           : 0.f;
                     }
+#pragma unroll
+                    for (int sp = 0; sp < 8; ++sp)
+#pragma unroll
+                        for (int u = 0; u < RB; ++u) acc[u] += v[sp][u];
 #pragma unroll
                     for (int u = 0; u < RB; ++u)
                         if (m + u < hi) finish(m + u, ch, acc[u], !bad);

@@ -657,7 +657,8 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(
 // =========================================================================================
 // State slicing at k (Figure 1(d)): FIR tail <- stage rows k+1 .. k+L-1, IIR state <- s_k,
 // and for several candidates the chosen candidate's k+1 block K/V rows into the cache;
-// then kv_len = kv_base + k + 1. Grid (B, blocks); every block strides over the work.
+// then kv_len = kv_base + k + 1. Grid (B, layers, blocks per layer): every layer's copy runs
+// in parallel, 16 bytes per thread where the rows allow it.
 // =========================================================================================
 template <typename T>
 __global__ void slice_kernel(const LayerDesc* __restrict__ layers, int n_layers, int d, int dh,
@@ -667,45 +668,43 @@ __global__ void slice_kernel(const LayerDesc* __restrict__ layers, int n_layers,
                              uint32_t* __restrict__ flags) {
     pdl_trigger();
     pdl_wait();
-    const int b = blockIdx.x;
+    const int b = blockIdx.x, li = blockIdx.y;
     const int k = kin[b];
     const int c = cin ? cin[b] : 0;
+    const bool first = li == 0 && blockIdx.z == 0 && threadIdx.x == 0;
     if (k < 0 || k > gamma || c < 0 || c >= C) {
-        if (blockIdx.y == 0 && threadIdx.x == 0) atomicOr(flags, (uint32_t)EVS_FLAG_BAD_K);
+        if (first) atomicOr(flags, (uint32_t)EVS_FLAG_BAD_K);
         return;
     }
     const int bc = b * C + c;
     const int n0 = kv_base[b];
-    const int stride = gridDim.y * blockDim.x;
-    const int start = blockIdx.y * blockDim.x + threadIdx.x;
-    bool overflow = n0 + k + 1 > t_max;
-    for (int li = 0; li < n_layers; ++li) {
-        const LayerDesc L = layers[li];
-        if (L.kind == EVS_LAYER_FIR) {
-            const int Lm1 = L.param - 1;
-            const float* st = L.stage + (size_t)bc * (Lm1 + Tb) * d;
-            for (int e = start; e < Lm1 * d; e += stride) {
-                const int j = e / d, ch = e % d;
-                L.tail[((size_t)b * Lm1 + j) * d + ch] = st[(size_t)(k + 1 + j) * d + ch];
-            }
-        } else if (L.kind == EVS_LAYER_IIR) {
-            const int n = d * L.param;
-            const float2* src = L.ret + ((size_t)bc * Tb + k) * n;
-            for (int e = start; e < n; e += stride) L.state[(size_t)b * n + e] = src[e];
-        } else if (C > 1 && !overflow) {
-            const int H = L.param;
-            const int per = (k + 1) * dh;
-            for (int e = start; e < H * per; e += stride) {
-                const int hh = e / per, r = e % per;
-                const int j = r / dh, x = r % dh;
-                const size_t src = ((((size_t)bc) * H + hh) * Tb + j) * dh + x;
-                const size_t dst = (((size_t)b * H + hh) * t_max + n0 + j) * dh + x;
-                ((T*)L.kc)[dst] = ((const T*)L.ks)[src];
-                ((T*)L.vc)[dst] = ((const T*)L.vs)[src];
-            }
+    const bool overflow = n0 + k + 1 > t_max;
+    const int stride = gridDim.z * blockDim.x;
+    const int start = blockIdx.z * blockDim.x + threadIdx.x;
+    const LayerDesc L = layers[li];
+    if (L.kind == EVS_LAYER_FIR) {
+        const int Lm1 = L.param - 1;
+        const float4* src = reinterpret_cast<const float4*>(L.stage + ((size_t)bc * (Lm1 + Tb) + k + 1) * d);
+        float4* dst = reinterpret_cast<float4*>(L.tail + (size_t)b * Lm1 * d);
+        for (int e = start; e < Lm1 * d / 4; e += stride) dst[e] = src[e];   // d % 64 == 0
+    } else if (L.kind == EVS_LAYER_IIR) {
+        const int n = d * L.param;                 // float2 elements, n even
+        const float4* src = reinterpret_cast<const float4*>(L.ret + ((size_t)bc * Tb + k) * n);
+        float4* dst = reinterpret_cast<float4*>(L.state + (size_t)b * n);
+        for (int e = start; e < n / 2; e += stride) dst[e] = src[e];
+    } else if (C > 1 && !overflow) {
+        const int H = L.param;
+        const int per = (k + 1) * dh;
+        for (int e = start; e < H * per; e += stride) {
+            const int hh = e / per, r = e % per;
+            const int j = r / dh, x = r % dh;
+            const size_t srci = ((((size_t)bc) * H + hh) * Tb + j) * dh + x;
+            const size_t dsti = (((size_t)b * H + hh) * t_max + n0 + j) * dh + x;
+            ((T*)L.kc)[dsti] = ((const T*)L.ks)[srci];
+            ((T*)L.vc)[dsti] = ((const T*)L.vs)[srci];
         }
     }
-    if (blockIdx.y == 0 && threadIdx.x == 0) {
+    if (first) {
         if (overflow) atomicOr(flags, (uint32_t)EVS_FLAG_KV_OVERFLOW);
         kv_len[b] = overflow ? t_max : n0 + k + 1;
     }
@@ -890,7 +889,7 @@ void launch_accept(evs_handle* h, const int32_t* tokens, const float* q, const f
 void launch_slice(evs_handle* h, const int32_t* k, const int32_t* cand) {
     prof_begin(h, EVS_K_SLICE);
     const evs_config& c = h->cfg;
-    dim3 grid(c.batch, 16);
+    dim3 grid(c.batch, c.n_layers, 8);
     if (is_bf16(h))
         launch_k(h, slice_kernel<bf16>, dim3(grid), dim3(256), 0, h->layer_dev, c.n_layers, c.d, c.head_dim, c.n_cand,
             c.gamma + 1, c.gamma, c.t_max, k, cand, h->kv_base, h->kv_len, h->flags);
