@@ -6,8 +6,12 @@
 // Swap-AB: the weight tile is the 128-row A operand and the tokens are the N dimension of
 // the MMA (16..256 per instruction, up to 512 in two accumulators), so the accumulator
 // D[n][m] sits in TMEM with one output channel per lane. One CTA owns a 128-channel tile
-// and a range of K; ranges of K are split across CTAs until the grid fills the 152 SMs,
-// and the last CTA to finish a tile adds the partial sums in a fixed order (deterministic).
+// and a range of K; ranges of K are split across CTAs until the grid fills the 152 SMs.
+// The splits of a tile form a thread-block cluster: each stores its fp32 partial tile to an
+// L2-resident scratch, and after one cluster barrier each adds a run of token rows over the
+// splits in a fixed order (deterministic). The in-projection of a FIR / IIR layer instead
+// pushes channel slices through distributed shared memory and runs the mixer in the
+// epilogue. Without a cluster, the last CTA to finish a tile adds the partial sums.
 //
 // Roles in a CTA of 128 threads: thread 0 issues TMA loads into a ring of stages, thread
 // 32 issues the MMAs and releases stages with tcgen05.commit, then all four warps read
@@ -33,9 +37,6 @@ constexpr int TC_A_BYTES = TC_BM * TC_BK * 2; // 16 KiB
 #ifndef EVS_TC_WIDE_NARROW
 #define EVS_TC_WIDE_NARROW 0  // narrow outputs split beyond one cluster on the global path
 #endif
-#ifndef EVS_TC_DSMEM_BATCH
-#define EVS_TC_DSMEM_BATCH 8  // token rows whose peer loads the cluster reduction keeps in flight
-#endif
 #ifndef EVS_TC_MAX_SPLITS
 #define EVS_TC_MAX_SPLITS 8
 #endif
@@ -56,8 +57,8 @@ constexpr int TC_SMEM_BUDGET = EVS_TC_SMEM_KB * 1024;
 struct TcArgs {
     float* Y;
     int ldy, M, N, kblocks, splits, n_pad, stages, accumulate, ncols, kbs;
-    int cluster;      // 1: the splits of a tile form a cluster and reduce through DSMEM
-    int park_rows;    // token rows parked per round of the cluster reduction
+    int cluster;      // 1: the splits of a tile form a cluster: partial tiles exchanged through
+                      // the scratch (part) and reduced by row runs after a cluster barrier
     float* part;      // [splits][M][N] partial sums when splits > 1
     int* counters;    // [N / 128] arrival counters, zero between launches
     uint32_t* flags;
@@ -97,7 +98,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     __shared__ volatile int abort_flag[1];
     __shared__ int last_flag[1];
     __shared__ float rinv_s[512];
-    __shared__ float red_s[4 * 512];
+    __shared__ __align__(16) float red_s[4 * 512];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const int b_bytes = p.n_pad * 128;
@@ -210,21 +211,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     pdl_wait();
     if (p.ssq_in && warp >= 2) {
         // 1/rms of each token row from the per-tile sums of squares of h, computed by the two
-        // warps that are idle during the mainloop: a row's tiles are spread over the lanes,
-        // eight rows' loads in flight before any is reduced
-        for (int m0 = (warp - 2) * 8; m0 < p.M; m0 += 16) {
-            float part[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
+        // warps that are idle during the mainloop: one row per lane (the loads of a tile are
+        // coalesced across the lanes), up to 32 tiles' loads in flight before any is summed
+        for (int m0 = (warp - 2) * 32; m0 < p.M; m0 += 64) {
+            const int m = m0 + lane;
+            if (m < p.M) {
                 float ss = 0.f;
-                if (m0 + u < p.M)
-                    for (int t = lane; t < p.ssq_tiles; t += 32) ss += p.ssq_in[(size_t)t * p.ssq_ld + m0 + u];
-                part[u] = ss;
-            }
+                for (int t0 = 0; t0 < p.ssq_tiles; t0 += 32) {
+                    float v[32];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float ss = warp_sum(part[u]);
-                if (lane == 0 && m0 + u < p.M) rinv_s[m0 + u] = rsqrtf(ss / (float)p.norm_d + 1e-6f);
+                    for (int u = 0; u < 32; ++u)
+                        v[u] = t0 + u < p.ssq_tiles ? p.ssq_in[(size_t)(t0 + u) * p.ssq_ld + m] : 0.f;
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) ss += v[u];
+                }
+                rinv_s[m] = rsqrtf(ss / (float)p.norm_d + 1e-6f);
             }
         }
     }
@@ -234,40 +235,110 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const bool bad = !ok || *abort_flag;
     if (bad && threadIdx.x == 0) atomicOr(p.flags, (uint32_t)EVS_FLAG_TIMEOUT);
     __syncthreads();
-    // One output value: row scale, store (or accumulate into the residual), bf16 copy, and
-    // this warp's share of the row's sum of squares. All lanes of a warp call it for the
-    // same m with consecutive channels nl.
-    auto finish = [&](int m, int nl, float v, bool live) {
+    // Rows of the fused K/V write: the destination offset of each token row (the channel's
+    // share added per thread), -1 past the end of the cache. Shares red_s with the sums of
+    // squares, which a K/V-writing launch never produces.
+    long long* kv_row = reinterpret_cast<long long*>(red_s);
+    const bool kv_ch = p.kv && n0 + (int)threadIdx.x >= p.d;   // this thread's channel is K or V
+    long long kv_col = 0;
+    __nv_bfloat16* kv_dst = nullptr;
+    if (p.kv) {
+        for (int m = threadIdx.x; m < p.M; m += blockDim.x) {
+            const int bc = m / p.kv_T, i = m % p.kv_T, b = bc / p.kv_C;
+            long long o;
+            if (p.kv_in_cache) {
+                const int t = p.kv_base[b] + i;
+                o = t < p.kv_tmax ? ((long long)b * p.kv_H * p.kv_tmax + t) * p.kv_dh : -1;
+            } else {
+                o = ((long long)bc * p.kv_H * p.kv_T + i) * p.kv_dh;
+            }
+            kv_row[m] = o;
+        }
+        if (kv_ch) {
+            const int c2 = n0 + (int)threadIdx.x - p.d, which = c2 / p.d, col = c2 % p.d;
+            const int hh = col / p.kv_dh, e = col % p.kv_dh;
+            kv_col = (long long)hh * (p.kv_in_cache ? p.kv_tmax : p.kv_T) * p.kv_dh + e;
+            kv_dst = p.kv_in_cache ? (which ? p.vc : p.kc) : (which ? p.vs : p.ks);
+        }
+        __syncthreads();
+    }
+    // The residual a row adds (0 without accumulation); callers load a batch of rows' values
+    // before finishing any of them.
+    auto resid = [&](int m, int nl) -> float {
+        return (p.accumulate && m < p.M) ? p.Y[(size_t)m * p.ldy + n0 + nl] : 0.f;
+    };
+    // One output value: row scale, store (plus the residual res), bf16 copy, and this warp's
+    // share of the row's sum of squares. All lanes of a warp call it for the same m with
+    // consecutive channels; nl is the calling thread's index.
+    auto finish = [&](int m, int nl, float v, float res, bool live) {
         if (p.ssq_in) v *= rinv_s[m];
         float out = v;
-        if (p.kv && n0 + nl >= p.d) {
+        if (kv_ch) {
             if (live) {
-                const int c2 = n0 + nl - p.d, which = c2 / p.d, col = c2 % p.d;
-                const int hh = col / p.kv_dh, e = col % p.kv_dh;
-                const int bc = m / p.kv_T, i = m % p.kv_T, b = bc / p.kv_C;
-                if (p.kv_in_cache) {
-                    const int t = p.kv_base[b] + i;
-                    if (t < p.kv_tmax)
-                        (which ? p.vc : p.kc)[(((size_t)b * p.kv_H + hh) * p.kv_tmax + t) * p.kv_dh + e] =
-                            __float2bfloat16_rn(out);
-                    else
-                        atomicOr(p.flags, (uint32_t)EVS_FLAG_KV_OVERFLOW);
-                } else {
-                    (which ? p.vs : p.ks)[(((size_t)bc * p.kv_H + hh) * p.kv_T + i) * p.kv_dh + e] =
-                        __float2bfloat16_rn(out);
-                }
+                const long long r = kv_row[m];
+                if (r >= 0)
+                    kv_dst[r + kv_col] = __float2bfloat16_rn(out);
+                else
+                    atomicOr(p.flags, (uint32_t)EVS_FLAG_KV_OVERFLOW);
             }
             return;
         }
         if (live) {
-            float* dst = p.Y + (size_t)m * p.ldy + n0 + nl;
-            if (p.accumulate) out += *dst;
-            *dst = out;
+            out += res;
+            p.Y[(size_t)m * p.ldy + n0 + nl] = out;
             if (p.hb_out) p.hb_out[(size_t)m * p.hb_ld + n0 + nl] = __float2bfloat16_rn(out);
         }
         if (p.ssq_out) {
             const float sq = warp_sum(live ? out * out : 0.f);
             if ((nl & 31) == 0) red_s[(nl >> 5) * 512 + m] = sq;
+        }
+    };
+    // Four consecutive channels 4*lane.. of one row (a warp covers the 128-channel row):
+    // float4 residual and stores, the row's sum of squares reduced within the warp.
+    const long long kv_col4 = [&]() -> long long {
+        if (!kv_ch) return 0;
+        const int c2 = n0 + 4 * lane - p.d, col = c2 % p.d;
+        return (long long)(col / p.kv_dh) * (p.kv_in_cache ? p.kv_tmax : p.kv_T) * p.kv_dh + col % p.kv_dh;
+    }();
+    auto resid4 = [&](int m) -> float4 {
+        return p.accumulate ? *reinterpret_cast<const float4*>(p.Y + (size_t)m * p.ldy + n0 + 4 * lane)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    auto finish4 = [&](int m, float4 v, float4 res, bool live) {
+        if (p.ssq_in) {
+            const float r = rinv_s[m];
+            v.x *= r; v.y *= r; v.z *= r; v.w *= r;
+        }
+        if (kv_ch) {
+            if (live) {
+                const long long r = kv_row[m];
+                if (r >= 0) {
+                    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+                    uint2 u;
+                    u.x = *reinterpret_cast<const uint32_t*>(&a);
+                    u.y = *reinterpret_cast<const uint32_t*>(&b);
+                    *reinterpret_cast<uint2*>(kv_dst + r + kv_col4) = u;
+                } else if (lane == 0) {
+                    atomicOr(p.flags, (uint32_t)EVS_FLAG_KV_OVERFLOW);
+                }
+            }
+            return;
+        }
+        float4 out = make_float4(v.x + res.x, v.y + res.y, v.z + res.z, v.w + res.w);
+        if (live) {
+            *reinterpret_cast<float4*>(p.Y + (size_t)m * p.ldy + n0 + 4 * lane) = out;
+            if (p.hb_out) {
+                const __nv_bfloat162 a = __floats2bfloat162_rn(out.x, out.y),
+                                     b = __floats2bfloat162_rn(out.z, out.w);
+                uint2 u;
+                u.x = *reinterpret_cast<const uint32_t*>(&a);
+                u.y = *reinterpret_cast<const uint32_t*>(&b);
+                *reinterpret_cast<uint2*>(p.hb_out + (size_t)m * p.hb_ld + n0 + 4 * lane) = u;
+            }
+        }
+        if (p.ssq_out) {
+            const float sq = warp_sum(live ? out.x * out.x + out.y * out.y + out.z * out.z + out.w * out.w : 0.f);
+            if (lane == 0) p.ssq_out[(size_t)tile * p.ssq_ld + m] = sq;
         }
     };
     int own_lo = 0, own_hi = 0;   // token rows whose sums of squares this CTA completes
@@ -277,33 +348,42 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // ---- in-projection + mixer: gather this CTA's channel slice of v for every token
         // row (whole tile without split-K; a 1/S share of the channels with a cluster), then
         // one thread per (sequence-candidate, channel) runs the FIR / modal IIR over time
-        float* park = reinterpret_cast<float*>(smem);            // [M][128] this CTA's partials
+        float* park = reinterpret_cast<float*>(smem);
         const int S = p.splits;
         const int c_lo = (int)(128LL * split / S), c_hi = (int)(128LL * (split + 1) / S);
         const int cw = c_hi - c_lo;
-        float* vals = S == 1 ? park : park + (size_t)p.M * TC_BM;   // [M][cw] final values
-        for (int c0 = 0; c0 < p.M; c0 += 16) {
-            float v[16];
-            tmem_ld16(trow + (uint32_t)c0, v);
+        const int cwm = (TC_BM + S - 1) / S;                         // slot row stride
+        // S == 1: park = [M][128] the whole tile; else park = [S][M][cwm] the partials of
+        // this CTA's channel slice as pushed by every rank, then vals = [M][cw] their sum
+        float* vals = S == 1 ? park : park + (size_t)S * p.M * cwm;
+        if (S == 1) {
+            for (int c0 = 0; c0 < p.M; c0 += 16) {
+                float v[16];
+                tmem_ld16(trow + (uint32_t)c0, v);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                if (c0 + j < p.M) park[(size_t)(c0 + j) * TC_BM + nl_lane] = v[j];
-        }
-        if (S > 1) {
-            cluster_sync();
-            const uint32_t base = smem_u32(park);
+                for (int j = 0; j < 16; ++j)
+                    if (c0 + j < p.M) park[(size_t)(c0 + j) * TC_BM + nl_lane] = v[j];
+            }
+        } else {
+            const int own = ((nl_lane + 1) * S - 1) / TC_BM;         // rank owning this channel
+            const int own_lo = (int)(128LL * own / S);
+            const uint32_t dst = map_peer(smem_u32(park), (uint32_t)own) +
+                                 (uint32_t)((size_t)split * p.M * cwm + nl_lane - own_lo) * 4u;
+            cluster_sync();                       // every rank's mainloop is done: rings free
+            for (int c0 = 0; c0 < p.M; c0 += 16) {
+                float v[16];
+                tmem_ld16(trow + (uint32_t)c0, v);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (c0 + j < p.M) st_peer_f32(dst + (uint32_t)((c0 + j) * cwm) * 4u, v[j]);
+            }
+            cluster_sync();                       // every push has landed
             for (int idx = threadIdx.x; idx < p.M * cw; idx += blockDim.x) {
                 const int m = idx / cw, c = idx % cw;
-                const uint32_t off = base + (uint32_t)(m * TC_BM + c_lo + c) * 4u;
-                float v[8];   // every peer's value requested before any is added (S <= 8)
-#pragma unroll
-                for (int sp = 0; sp < 8; ++sp) v[sp] = sp < S ? ld_peer_f32(map_peer(off, (uint32_t)sp)) : 0.f;
                 float acc = 0.f;
-#pragma unroll
-                for (int sp = 0; sp < 8; ++sp) acc += v[sp];
+                for (int sp = 0; sp < S; ++sp) acc += park[((size_t)sp * p.M + m) * cwm + c];
                 vals[idx] = acc;
             }
-            cluster_sync();                       // peers finished reading this CTA's park
         }
         __syncthreads();
         const int vld = S == 1 ? TC_BM : cw;      // row stride of vals
@@ -375,65 +455,48 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
     } else if (p.splits == 1) {
         for (int c0 = 0; c0 < p.M; c0 += 16) {
+            float v[16], r[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) r[j] = resid(c0 + j, nl_lane);
+            tmem_ld16(trow + (uint32_t)c0, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (c0 + j < p.M) finish(c0 + j, nl_lane, v[j], r[j], !bad);
+        }
+        own_hi = p.M;
+    } else if (p.cluster) {
+        // split-K within the cluster through L2: every rank stores its partial tile to the
+        // scratch, one cluster barrier, then each rank adds a run of rows over the ranks in
+        // rank order (deterministic) and finishes them: a row per warp, four channels a lane
+        const int S = p.splits;
+        float* mine = p.part + ((size_t)tile * S + split) * p.M * TC_BM;
+        for (int c0 = 0; c0 < p.M; c0 += 16) {
             float v[16];
             tmem_ld16(trow + (uint32_t)c0, v);
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                if (c0 + j < p.M) finish(c0 + j, nl_lane, v[j], !bad);
+                if (c0 + j < p.M) mine[(size_t)(c0 + j) * TC_BM + nl_lane] = v[j];
         }
-        own_hi = p.M;
-    } else if (p.cluster) {
-        // split-K through distributed shared memory: the CTAs of the cluster park their
-        // partial tiles in their own (now idle) rings, a chunk of token rows at a time; CTA r
-        // sums its share of each chunk's rows across the cluster in a fixed order
-        float* park = reinterpret_cast<float*>(smem);
-        const uint32_t base = smem_u32(park);
-        const int ch = threadIdx.x;               // channel within the tile
-        const int r = split;                      // rank in the cluster (cluster spans y)
-        for (int c_lo = 0; c_lo < p.M; c_lo += p.park_rows) {
-            const int cnt = min(p.park_rows, p.M - c_lo);
-            for (int c0 = 0; c0 < cnt; c0 += 16) {
-                float v[16];
-                tmem_ld16(trow + (uint32_t)(c_lo + c0), v);
+        cluster_sync();                           // every rank's partial tile is in L2
+        const int per = (p.M + S - 1) / S;
+        const int lo = split * per, hi = min(p.M, lo + per);
+        const float* base = p.part + (size_t)tile * S * p.M * TC_BM;
+        for (int m = lo + warp; m < hi; m += 4) {
+            const float4 res = resid4(m);
+            float4 x[8];
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (c0 + j < cnt) park[(size_t)(c0 + j) * TC_BM + nl_lane] = v[j];
+            for (int sp = 0; sp < 8; ++sp)
+                x[sp] = sp < S ? __ldcg(reinterpret_cast<const float4*>(base + ((size_t)sp * p.M + m) * TC_BM) + lane)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 acc = x[0];
+#pragma unroll
+            for (int sp = 1; sp < 8; ++sp) {
+                acc.x += x[sp].x;
+                acc.y += x[sp].y;
+                acc.z += x[sp].z;
+                acc.w += x[sp].w;
             }
-            cluster_sync();
-            const int lo = c_lo + (int)((long long)cnt * r / p.splits);
-            const int hi = c_lo + (int)((long long)cnt * (r + 1) / p.splits);
-            // RB rows' peer loads in flight at once; batching pays only with many rows
-            auto reduce_rows = [&](auto rb_tag) {
-                constexpr int RB = decltype(rb_tag)::value;
-                for (int m = lo; m < hi; m += RB) {
-                    float acc[RB];
-#pragma unroll
-                    for (int u = 0; u < RB; ++u) acc[u] = 0.f;
-                    // all peers' values for RB rows requested before any is added (splits <= 8)
-                    float v[8][RB];
-#pragma unroll
-                    for (int sp = 0; sp < 8; ++sp) {
-                        const uint32_t peer = map_peer(base, (uint32_t)(sp < p.splits ? sp : 0));
-#pragma unroll
-                        for (int u = 0; u < RB; ++u)
-                            v[sp][u] = (sp < p.splits && m + u < hi)
-                                           ? ld_peer_f32(peer + (uint32_t)((m + u - c_lo) * TC_BM + ch) * 4u)
-                                           : 0.f;
-                    }
-#pragma unroll
-                    for (int sp = 0; sp < 8; ++sp)
-#pragma unroll
-                        for (int u = 0; u < RB; ++u) acc[u] += v[sp][u];
-#pragma unroll
-                    for (int u = 0; u < RB; ++u)
-                        if (m + u < hi) finish(m + u, ch, acc[u], !bad);
-                }
-            };
-            if (hi - lo >= 16)
-                reduce_rows(std::integral_constant<int, EVS_TC_DSMEM_BATCH>{});
-            else
-                reduce_rows(std::integral_constant<int, 1>{});
-            cluster_sync();                       // peers finished reading this chunk
+            finish4(m, acc, res, !bad);
         }
     } else {
         const int n = n0 + nl_lane;
@@ -455,7 +518,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             __threadfence();
             // four rows at a time, every split's value requested before any is summed
             for (int m0 = 0; m0 < p.M; m0 += 4) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                float acc[4] = {0.f, 0.f, 0.f, 0.f}, rv[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) rv[u] = resid(m0 + u, nl_lane);
                 for (int sp = 0; sp < p.splits; ++sp) {
                     float v[4];
 #pragma unroll
@@ -466,28 +531,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                    if (m0 + u < p.M) finish(m0 + u, nl_lane, acc[u], !bad);
+                    if (m0 + u < p.M) finish(m0 + u, nl_lane, acc[u], rv[u], !bad);
             }
             if (threadIdx.x == 0) p.counters[tile] = 0;
             own_hi = p.M;
         }
     }
-    if (p.ssq_out) {
+    if (p.ssq_out && !(p.splits > 1 && p.cluster)) {
         __syncthreads();
         auto put = [&](int lo, int hi) {
             for (int m = lo + threadIdx.x; m < hi; m += blockDim.x)
                 p.ssq_out[(size_t)tile * p.ssq_ld + m] =
                     red_s[m] + red_s[512 + m] + red_s[1024 + m] + red_s[1536 + m];
         };
-        if (p.splits > 1 && p.cluster) {
-            for (int c_lo = 0; c_lo < p.M; c_lo += p.park_rows) {
-                const int cnt = min(p.park_rows, p.M - c_lo);
-                put(c_lo + (int)((long long)cnt * split / p.splits),
-                    c_lo + (int)((long long)cnt * (split + 1) / p.splits));
-            }
-        } else {
-            put(own_lo, own_hi);
-        }
+        put(own_lo, own_hi);   // (the cluster path wrote its rows' sums directly)
     }
     tc_fence_before();
     __syncthreads();
@@ -559,7 +616,7 @@ int tc_splits(int N, int K) {
 // Launch shape of one projection: token padding, split-K, k-blocks per stage, ring depth,
 // TMEM columns and dynamic shared memory.
 struct TcShape {
-    int n_pad, tiles, kblocks, splits, kbs, stages, ncols, cluster, M_for_park, park_rows;
+    int n_pad, tiles, kblocks, splits, kbs, stages, ncols, cluster;
     size_t smem;
 };
 
@@ -568,9 +625,9 @@ static size_t tc_part_floats(const TcShape& t, int M, int N) {
     return (t.splits > 1 && !t.cluster) ? (size_t)t.splits * M * N : 0;
 }
 
-static TcShape tc_shape(int M, int N, int K, size_t part_cap = (size_t)-1, int max_splits = 1 << 30) {
+static TcShape tc_shape(int M, int N, int K, size_t part_cap = (size_t)-1, int max_splits = 1 << 30,
+                        bool allow_cluster = true) {
     TcShape t{};
-    t.M_for_park = M;
     // tokens padded to the MMA's N granularity; above 256 two accumulators of 256 columns
     t.n_pad = M > 256 ? 512 : (M + 15) / 16 * 16;
     t.tiles = N / TC_BM;
@@ -588,15 +645,13 @@ static TcShape tc_shape(int M, int N, int K, size_t part_cap = (size_t)-1, int m
     t.ncols = 32;
     while (t.ncols < t.n_pad) t.ncols <<= 1;
     t.smem = (size_t)t.stages * t.kbs * kb_bytes + 1024 + (2 * t.stages + 1) * 8;
-    // cluster reduction when the splits fit a portable cluster and the partial tile fits the ring
-    // the cluster reduction parks [rows][128] fp32 partial tiles in the ring, as many token
-    // rows at a time as fit (a multiple of 16)
-    t.park_rows = (int)(((size_t)t.stages * t.kbs * kb_bytes / (TC_BM * 4)) / 16 * 16);
-    t.cluster = t.splits > 1 && t.splits <= 8 && t.park_rows >= 16;
+    // cluster reduction when the splits fit a portable cluster and the scratch holds every
+    // partial tile of the launch
+    t.cluster = allow_cluster && t.splits > 1 && t.splits <= 8 && (size_t)N * t.splits * M <= part_cap;
     if (tc_part_floats(t, M, N) > part_cap && t.splits > 1) {
         // scratch too small for this many partial tiles: fewer splits
         int s = (int)(part_cap / ((size_t)M * N));
-        return tc_shape(M, N, K, part_cap, s < 1 ? 1 : s);
+        return tc_shape(M, N, K, part_cap, s < 1 ? 1 : s, allow_cluster);
     }
     return t;
 }
@@ -635,7 +690,10 @@ bool gemm_tc_supported(int M, int N, int K) {
 bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, float* Y, int M, int N, int K,
                     int ldy, int accumulate, const GemmFuse* fz, int* fused) {
     if (fused) *fused = 0;
-    const TcShape t = tc_shape(M, N, K, h->gemm_part_floats);
+    // the cluster reduction finishes four channels per lane with 16-byte stores
+    const bool vec_ok = ((uintptr_t)Y % 16 == 0) && ldy % 4 == 0 &&
+                        (!fz || !fz->hb_out || ((uintptr_t)fz->hb_out % 8 == 0 && fz->hb_ld % 4 == 0));
+    const TcShape t = tc_shape(M, N, K, h->gemm_part_floats, 1 << 30, vec_ok);
     CUtensorMap ta, tb;
 #if EVS_TC_PACKED
     if (!make_map(&ta, W, (uint64_t)N * K / TC_BK, (uint64_t)TC_BK, TC_BM)) return false;
@@ -647,7 +705,7 @@ bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, flo
     TcArgs a{};
     a.Y = Y; a.ldy = ldy; a.M = M; a.N = N; a.kblocks = t.kblocks; a.splits = t.splits; a.n_pad = t.n_pad;
     a.stages = t.stages; a.accumulate = accumulate; a.ncols = t.ncols; a.kbs = t.kbs; a.cluster = t.cluster;
-    a.park_rows = t.park_rows; a.part = h->gemm_part; a.counters = h->gemm_counters; a.flags = h->flags;
+    a.part = h->gemm_part; a.counters = h->gemm_counters; a.flags = h->flags;
     a.d = h->cfg.d;
     int did = 0;
     if (fz) {
@@ -666,7 +724,7 @@ bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, flo
             const LayerDesc& L = h->layer[fz->mix_layer];
             const evs_layer_weights& LW = h->w.layer[fz->mix_layer];
             const int cw = (TC_BM + t.splits - 1) / t.splits;
-            const size_t need = (size_t)M * TC_BM * 4 + (t.splits > 1 ? (size_t)M * cw * 4 : 0);
+            const size_t need = t.splits > 1 ? (size_t)(t.splits + 1) * M * cw * 4 : (size_t)M * TC_BM * 4;
             const bool shape_ok = (t.splits == 1 || t.cluster) && need <= ring && M % ps->T == 0 &&
                                   (L.kind == EVS_LAYER_FIR || 32 % L.param == 0);
             if (shape_ok) {
@@ -687,7 +745,7 @@ bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, flo
                 did |= 1;
             }
         }
-        if (fz->kv_layer >= 0 && ps) {
+        if (fz->kv_layer >= 0 && ps && !fz->ssq_out) {   // the row table shares the ssq scratch
             const LayerDesc& L = h->layer[fz->kv_layer];
             a.kv = 1;
             a.kv_H = L.param;
@@ -771,7 +829,7 @@ extern "C" evs_status evs_projection_noalloc(const void* X, int32_t x_rows, cons
     TcArgs a{};
     a.Y = Y; a.ldy = ldy; a.M = M; a.N = N; a.kblocks = t.kblocks; a.splits = t.splits; a.n_pad = t.n_pad;
     a.stages = t.stages; a.accumulate = accumulate; a.ncols = t.ncols; a.kbs = t.kbs; a.cluster = t.cluster;
-    a.park_rows = t.park_rows; a.part = sc->part; a.counters = sc->counters; a.flags = &sc->flags;
+    a.part = sc->part; a.counters = sc->counters; a.flags = &sc->flags;
     if (!launch_tc(t, ta, tb, a, s, false)) return EVS_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? EVS_OK : EVS_ERR_CUDA;
 }
