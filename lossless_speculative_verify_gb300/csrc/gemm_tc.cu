@@ -209,6 +209,44 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     // ---- epilogue: lane = output channel, columns = tokens ---------------------------------
     pdl_wait();
+    // Mixer of a FIR / IIR in-projection: this CTA's channel slice [mc_lo, mc_lo + mcw) (the
+    // whole tile without split-K). The parameters and carried state of each thread's first
+    // items are loaded here, while the mainloop still runs.
+    const int mc_lo = (int)(128LL * split / p.splits);
+    const int mcw = (int)(128LL * (split + 1) / p.splits) - mc_lo;
+    const int mT = p.mix_T > 0 ? p.mix_T : 1, mgroups = p.M / mT;
+    // FIR item: one (sequence-candidate g, channel) pair; taps w[j] and the history
+    // prev[j] = x_{-1-j} (the newest carried input first), zero past the filter length
+    auto fir_load = [&](int pair, float (&w)[16], float (&prev)[15]) {
+        const int L = p.mix_param;
+        const bool on = pair < mgroups * mcw;
+        const int g = on ? pair / mcw : 0, n = n0 + mc_lo + (on ? pair % mcw : 0), b = g / p.mix_C;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) w[j] = (on && j < L) ? p.taps[(size_t)n * L + j] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 15; ++j)
+            prev[j] = (on && j < L - 1) ? p.tail[((size_t)b * (L - 1) + (L - 2 - j)) * p.d + n] : 0.f;
+    };
+    // IIR item: one (g, channel, pole); pole lambda, input weight B, readout weight C, state
+    auto iir_load = [&](int it, float2& l, float2& bq, float2& cq, float2& sv) {
+        const int N = p.mix_param;
+        l = bq = cq = sv = make_float2(0.f, 0.f);
+        if (it < mgroups * mcw * N) {
+            const int k = it % N, n = n0 + mc_lo + (it / N) % mcw, b = (it / (N * mcw)) / p.mix_C;
+            l = p.lam[(size_t)n * N + k];
+            bq = p.bq[(size_t)n * N + k];
+            cq = p.cq[(size_t)n * N + k];
+            sv = p.state[((size_t)b * p.d + n) * N + k];
+        }
+    };
+    float fw[16], fprev[15];
+    float2 il0, ib0, ic0, is0, il1, ib1, ic1, is1;
+    if (p.mix == 1) {
+        fir_load(threadIdx.x, fw, fprev);
+    } else if (p.mix == 2) {
+        iir_load(threadIdx.x, il0, ib0, ic0, is0);
+        iir_load(threadIdx.x + blockDim.x, il1, ib1, ic1, is1);
+    }
     if (p.ssq_in && warp >= 2) {
         // 1/rms of each token row from the per-tile sums of squares of h, computed by the two
         // warps that are idle during the mainloop: one row per lane (the loads of a tile are
@@ -390,67 +428,81 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int T = p.mix_T, groups = p.M / T;
         const int voff = S == 1 ? c_lo : 0;       // column of this CTA's first channel in vals
         if (p.mix == 1 && !bad) {
-            // FIR: one thread per (sequence-candidate, channel)
+            // FIR: one thread per (sequence-candidate, channel), y_t = sum_j w_j x_{t-j}
+            const int L = p.mix_param;
             for (int pair = threadIdx.x; pair < groups * cw; pair += blockDim.x) {
+                if (pair != (int)threadIdx.x) fir_load(pair, fw, fprev);
                 const int g = pair / cw, c = pair % cw, n = n0 + c_lo + c, b = g / p.mix_C;
                 const float* vrow = vals + (size_t)g * T * vld + voff + c;
-                const int L = p.mix_param;
-                float w[16], hist[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    w[j] = (j < L) ? p.taps[(size_t)n * L + j] : 0.f;
-                    hist[j] = (j < L - 1) ? p.tail[((size_t)b * (L - 1) + j) * p.d + n] : 0.f;
-                }
                 float* st = p.stage + (size_t)g * (L - 1 + T) * p.d;
-                if (!p.mix_commit)
-                    for (int j = 0; j < L - 1; ++j) st[(size_t)j * p.d + n] = hist[j];
-                for (int t = 0; t < T; ++t) {
-                    const float v = vrow[(size_t)t * vld] * (p.ssq_in ? rinv_s[g * T + t] : 1.f);
-                    float y = w[0] * v;
-#pragma unroll
-                    for (int j = 1; j < 16; ++j)
-                        if (j < L) y = fmaf(w[j], hist[L - 1 - j], y);
+                if (!p.mix_commit) {
 #pragma unroll
                     for (int j = 0; j < 15; ++j)
-                        if (j < L - 2) hist[j] = hist[j + 1];
-                    hist[L - 2] = v;
+                        if (j < L - 1) st[(size_t)(L - 2 - j) * p.d + n] = fprev[j];
+                }
+                for (int t = 0; t < T; ++t) {
+                    const float v = vrow[(size_t)t * vld] * (p.ssq_in ? rinv_s[g * T + t] : 1.f);
+                    float y = fw[0] * v;
+#pragma unroll
+                    for (int j = 1; j < 16; ++j)
+                        if (j < L) y = fmaf(fw[j], fprev[j - 1], y);
+#pragma unroll
+                    for (int j = 14; j > 0; --j) fprev[j] = fprev[j - 1];
+                    fprev[0] = v;
                     p.mix_out[((size_t)g * T + t) * p.d + n] = __float2bfloat16_rn(y);
                     if (!p.mix_commit) st[(size_t)(L - 1 + t) * p.d + n] = v;
                 }
-                if (p.mix_commit)
-                    for (int j = 0; j < L - 1; ++j) p.tail[((size_t)b * (L - 1) + j) * p.d + n] = hist[j];
+                if (p.mix_commit) {
+#pragma unroll
+                    for (int j = 0; j < 15; ++j)
+                        if (j < L - 1) p.tail[((size_t)b * (L - 1) + (L - 2 - j)) * p.d + n] = fprev[j];
+                }
             }
         } else if (p.mix == 2) {
             // modal IIR: N consecutive lanes hold the N poles of one channel (N divides 32),
-            // the readout summed by a shuffle reduction over them
+            // the readout summed by a shuffle reduction over them; two items per thread at a
+            // time (it and it + blockDim.x), their recurrences interleaved
             const int N = p.mix_param;
             const int items = groups * cw * N;                    // (group, channel, pole)
             const int span = (items + 31) / 32 * 32;              // whole warps take part
-            for (int it = threadIdx.x; it < span; it += blockDim.x) {
-                const bool on = it < items && !bad;
-                const int k = it % N, c = (it / N) % cw, g = min(it / (N * cw), groups - 1);
-                const int n = n0 + c_lo + c, b = g / p.mix_C;
-                const float* vrow = vals + (size_t)g * T * vld + voff + c;
-                float2 l = make_float2(0.f, 0.f), bq = l, cq = l, sv = l;
-                if (on) {
-                    l = p.lam[(size_t)n * N + k];
-                    bq = p.bq[(size_t)n * N + k];
-                    cq = p.cq[(size_t)n * N + k];
-                    sv = p.state[((size_t)b * p.d + n) * N + k];
+            const int nt = blockDim.x;
+            for (int it = threadIdx.x; it < span; it += 2 * nt) {
+                if (it != (int)threadIdx.x) {
+                    iir_load(it, il0, ib0, ic0, is0);
+                    iir_load(it + nt, il1, ib1, ic1, is1);
                 }
+                const bool on0 = it < items && !bad, on1 = it + nt < items && !bad;
+                const int k0 = it % N, c0 = (it / N) % cw, g0 = min(it / (N * cw), groups - 1);
+                const int k1 = (it + nt) % N, c1 = ((it + nt) / N) % cw, g1 = min((it + nt) / (N * cw), groups - 1);
+                const int n_0 = n0 + c_lo + c0, n_1 = n0 + c_lo + c1;
+                const float* vr0 = vals + (size_t)g0 * T * vld + voff + c0;
+                const float* vr1 = vals + (size_t)g1 * T * vld + voff + c1;
                 for (int t = 0; t < T; ++t) {
-                    const float u = on ? vrow[(size_t)t * vld] * (p.ssq_in ? rinv_s[g * T + t] : 1.f) : 0.f;
-                    const float sx = fmaf(l.x, sv.x, fmaf(-l.y, sv.y, bq.x * u));
-                    const float sy = fmaf(l.x, sv.y, fmaf(l.y, sv.x, bq.y * u));
-                    sv = make_float2(sx, sy);
-                    float part = fmaf(cq.x, sx, -cq.y * sy);
-                    for (int o = N >> 1; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-                    if (on) {
-                        if (k == 0) p.mix_out[((size_t)g * T + t) * p.d + n] = __float2bfloat16_rn(part);
-                        if (!p.mix_commit) p.ret[(((size_t)g * T + t) * p.d + n) * N + k] = sv;
+                    const float u0 = on0 ? vr0[(size_t)t * vld] * (p.ssq_in ? rinv_s[g0 * T + t] : 1.f) : 0.f;
+                    const float u1 = on1 ? vr1[(size_t)t * vld] * (p.ssq_in ? rinv_s[g1 * T + t] : 1.f) : 0.f;
+                    is0 = make_float2(fmaf(il0.x, is0.x, fmaf(-il0.y, is0.y, ib0.x * u0)),
+                                      fmaf(il0.x, is0.y, fmaf(il0.y, is0.x, ib0.y * u0)));
+                    is1 = make_float2(fmaf(il1.x, is1.x, fmaf(-il1.y, is1.y, ib1.x * u1)),
+                                      fmaf(il1.x, is1.y, fmaf(il1.y, is1.x, ib1.y * u1)));
+                    float q0 = fmaf(ic0.x, is0.x, -ic0.y * is0.y);
+                    float q1 = fmaf(ic1.x, is1.x, -ic1.y * is1.y);
+                    for (int o = N >> 1; o > 0; o >>= 1) {
+                        q0 += __shfl_xor_sync(0xffffffffu, q0, o);
+                        q1 += __shfl_xor_sync(0xffffffffu, q1, o);
+                    }
+                    if (on0) {
+                        if (k0 == 0) p.mix_out[((size_t)g0 * T + t) * p.d + n_0] = __float2bfloat16_rn(q0);
+                        if (!p.mix_commit) p.ret[(((size_t)g0 * T + t) * p.d + n_0) * N + k0] = is0;
+                    }
+                    if (on1) {
+                        if (k1 == 0) p.mix_out[((size_t)g1 * T + t) * p.d + n_1] = __float2bfloat16_rn(q1);
+                        if (!p.mix_commit) p.ret[(((size_t)g1 * T + t) * p.d + n_1) * N + k1] = is1;
                     }
                 }
-                if (on && p.mix_commit) p.state[((size_t)b * p.d + n) * N + k] = sv;
+                if (p.mix_commit) {
+                    if (on0) p.state[((size_t)(g0 / p.mix_C) * p.d + n_0) * N + k0] = is0;
+                    if (on1) p.state[((size_t)(g1 / p.mix_C) * p.d + n_1) * N + k1] = is1;
+                }
             }
         }
     } else if (p.splits == 1) {
