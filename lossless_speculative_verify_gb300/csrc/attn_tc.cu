@@ -1,6 +1,7 @@
 // Split-KV causal attention over the readable KV prefix on tcgen05 tensor cores.
 //
-// One CTA per (prefix chunk, sequence x head). All queries of the sequence (every block
+// One CTA per (prefix chunk, sequence x head); the chunks are equal shares of the key tiles
+// of the sequence's readable prefix, worked out from its length at run time. All queries of the sequence (every block
 // position of every candidate: they share the prefix) are the N dimension of the MMAs, so
 // each TMA-staged 128-key tile of K and V is read from HBM once and used by every query.
 //   S^T[key][q] = K_tile . Q^T          (A = K tile, K-major; B = Q, K-major; D in TMEM)
@@ -55,9 +56,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     const int b = bh / a.H, head = bh % a.H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = a.kv_base[b];
-    const int k_lo = split * a.tiles * AT_KEYS;
-    const int k_hi = min(k_lo + a.tiles * AT_KEYS, n);
-    const int ntiles = k_hi > k_lo ? (k_hi - k_lo + AT_KEYS - 1) / AT_KEYS : 0;
+    // this CTA's equal share of the readable prefix's key tiles (at most a.tiles of them)
+    const int nt_all = (n + AT_KEYS - 1) / AT_KEYS;
+    const int t_lo = (int)((long long)nt_all * split / a.splits);
+    const int t_hi = (int)((long long)nt_all * (split + 1) / a.splits);
+    const int ntiles = min(t_hi - t_lo, a.tiles);
+    const int k_lo = t_lo * AT_KEYS;
+    const int k_hi = min(k_lo + ntiles * AT_KEYS, n);
     float* part = a.part + (((size_t)bh * a.splits + split) * a.q_stride) * (AT_DH + 2);
 
     if (ntiles == 0) {  // chunk past the readable prefix: empty partial
@@ -275,7 +280,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 attn_encode_fn() {
 }
 
 // KV cache [B*H][t_max][128] bf16 as a 3-D map with a 64 x 128-key box, 128-byte swizzle.
-static bool make_kv_map(CUtensorMap* m, const void* base, int t_max, int bh) {
+bool make_kv_map(CUtensorMap* m, const void* base, int t_max, int bh) {
     auto fn = attn_encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)AT_DH, (cuuint64_t)t_max, (cuuint64_t)bh};
@@ -289,6 +294,10 @@ static bool make_kv_map(CUtensorMap* m, const void* base, int t_max, int bh) {
 
 // Chunking of the prefix for a pass with Q queries per sequence (dh = 128, bf16).
 AttnPlan attn_tc_plan(int Q, int B, int H, int t_max, int smem_max) {
+    if (Q > 16) {   // many queries: the streaming kernel with one query per TMEM lane
+        const AttnPlan f = attn_fa_plan(Q, B, H, t_max, smem_max);
+        if (f.ok) return f;
+    }
     AttnPlan p{};
     p.n_q = (Q + 15) / 16 * 16;
     if (Q < 1 || p.n_q > 128) return p;
@@ -298,14 +307,30 @@ AttnPlan attn_tc_plan(int Q, int B, int H, int t_max, int smem_max) {
     if (tmax > p_cap) tmax = p_cap;
     if (tmax > 16) tmax = 16;
     if (tmax < 1) return p;
-    // enough chunks that splits x sequences x heads covers the SMs about twice
+    // Chunks are dealt out at run time in equal shares of the readable prefix (see the
+    // kernel), so the plan fixes only the number of splits and the largest share. Prefer one
+    // wave of two CTAs per SM (TMEM and shared memory permitting); past tmax tiles per CTA,
+    // as many splits of tmax tiles as the cache needs.
     const long long total_tiles = (t_max + AT_KEYS - 1) / AT_KEYS;
-    const long long want = (2LL * 152 + (long long)B * H - 1) / ((long long)B * H);
-    long long per = (total_tiles + want - 1) / want;
-    if (per < 1) per = 1;
-    if (per > tmax) per = tmax;
+    const long long bh = (long long)B * H;
+    auto fits_two = [&](long long per) {
+        const long long fixed = 1024 + 2LL * p.n_q * 128 + per * 2 * p.n_q * 128 + 64 * 8;
+        return (per + 1) * p.n_q <= 256 && fixed + 2LL * AT_TILE_BYTES <= 110 * 1024;
+    };
+    long long splits = 304 / bh;
+    if (splits < 1) splits = 1;
+    long long per = (total_tiles + splits - 1) / splits;
+    if (per <= tmax && !fits_two(per)) {          // one wave of one CTA per SM instead
+        splits = 152 / bh;
+        if (splits < 1) splits = 1;
+        per = (total_tiles + splits - 1) / splits;
+    }
+    if (per > tmax) {
+        per = tmax;
+        splits = (total_tiles + per - 1) / per;
+    }
     p.tiles = (int)per;
-    p.splits = (int)((total_tiles + per - 1) / per);
+    p.splits = (int)splits;
     int need = (p.tiles + 1) * p.n_q;
     p.ncols = 32;
     while (p.ncols < need) p.ncols <<= 1;
@@ -337,6 +362,7 @@ int attn_tc_init() {
 }
 
 bool launch_attn_tc(evs_handle* h, int li, const Pass& p, const AttnPlan& plan) {
+    if (plan.fa) return launch_attn_fa(h, li, p, plan);
     const LayerDesc& L = h->layer[li];
     const int H = L.param;
     CUtensorMap tk, tv;

@@ -361,7 +361,7 @@ evs_status evs_create(const evs_config* cfg, const evs_weights* weights, void* w
     h->fused = cfg->dtype == EVS_DTYPE_BF16 && cfg->d % 128 == 0 && cfg->vocab % 128 == 0 && h->g.M_max <= 512;
     if (cfg->dtype == EVS_DTYPE_BF16) {
         h->tc_smem_max = evs::gemm_tc_init();
-        const int attn_smem = evs::attn_tc_init();
+        const int attn_smem = std::min(evs::attn_tc_init(), evs::attn_fa_init());
         if (h->tc_smem_max < 0 || attn_smem < 0) {
             free(h);
             return EVS_ERR_CUDA;

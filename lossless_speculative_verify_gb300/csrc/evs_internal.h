@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -35,7 +36,8 @@ struct Geometry {
 
 // Prefix chunking of the tensor-core attention for one pass shape (attn_tc.cu).
 struct AttnPlan {
-    int ok;          // 1 if the tensor-core kernel takes this pass
+    int ok;          // 1 if a tensor-core kernel takes this pass
+    int fa;          // 1: queries on the TMEM lanes, online softmax (attn_fa.cu)
     int n_q;         // queries padded to 16 (MMA N)
     int tiles;       // 128-key tiles per CTA
     int splits;      // chunks covering t_max keys
@@ -131,6 +133,11 @@ int tc_cta_target();
 AttnPlan attn_tc_plan(int Q, int B, int H, int t_max, int smem_max);
 int attn_tc_init();
 bool launch_attn_tc(evs_handle* h, int layer, const Pass& p, const AttnPlan& plan);
+AttnPlan attn_fa_plan(int Q, int B, int H, int t_max, int smem_max);
+int attn_fa_init();
+bool launch_attn_fa(evs_handle* h, int layer, const Pass& p, const AttnPlan& plan);
+// 3-D tensor map over a [bh][t_max][128] bf16 K or V cache, boxes of 128 rows x 64 columns
+bool make_kv_map(CUtensorMap* m, const void* base, int t_max, int bh);
 bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, float* Y, int M, int N,
                     int K, int ldy, int accumulate, const GemmFuse* fz = nullptr, int* fused = nullptr);
 void launch_fir(evs_handle* h, int layer, const Pass& p);

@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(256) attn_split_kernel(
 constexpr int CMB_MAX_SPLITS = 1024;
 
 template <typename T>
-__global__ void __launch_bounds__(128) attn_combine_kernel(
+__global__ void __launch_bounds__(128, 4) attn_combine_kernel(
     const float* __restrict__ Y, int ldy, const T* __restrict__ kc, const T* __restrict__ vc,
     const T* __restrict__ ks, const T* __restrict__ vs, int H, int dh, int C, int Tb, int Q, int q_max,
     int t_max, int splits, int chunk, int in_cache, const int32_t* __restrict__ kv_base,
@@ -369,7 +369,9 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
     const int n = kv_base[b];  // rows n + j past t_max were never written (overflow flag set);
                                // their reads are clamped to stay in bounds
-    const int used = min(min((n + chunk - 1) / chunk, splits), CMB_MAX_SPLITS);
+    // chunk > 0: fixed chunks, the first ceil(n / chunk) splits hold keys; chunk == 0: the
+    // prefix is shared out over every split (empty ones report m = -inf)
+    const int used = min(chunk > 0 ? min((n + chunk - 1) / chunk, splits) : splits, CMB_MAX_SPLITS);
     const float* pbase = part + (((size_t)b * H + hh) * splits * q_max + qi) * (dh + 2);
     const size_t pstride = (size_t)q_max * (dh + 2);
     float M = -INFINITY;
@@ -409,15 +411,17 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(
     for (int e = tid; e < dh; e += blockDim.x) {
         float O = 0.f;
         int s = 0;
-        for (; s + 4 <= used; s += 4) {
-            const float a0 = pbase[(s + 0) * pstride + e], a1 = pbase[(s + 1) * pstride + e];
-            const float a2 = pbase[(s + 2) * pstride + e], a3 = pbase[(s + 3) * pstride + e];
-            O = fmaf(a0, w_s[s], O);
-            O = fmaf(a1, w_s[s + 1], O);
-            O = fmaf(a2, w_s[s + 2], O);
-            O = fmaf(a3, w_s[s + 3], O);
+        // splits of weight 0 (empty, or negligible) are skipped: an empty split leaves its o
+        // unwritten. Eight splits' loads in flight before any is summed.
+        for (; s + 8 <= used; s += 8) {
+            float a8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) a8[u] = w_s[s + u] != 0.f ? pbase[(s + u) * pstride + e] : 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) O = fmaf(a8[u], w_s[s + u], O);
         }
-        for (; s < used; ++s) O = fmaf(pbase[s * pstride + e], w_s[s], O);
+        for (; s < used; ++s)
+            if (w_s[s] != 0.f) O = fmaf(pbase[s * pstride + e], w_s[s], O);
         for (int j = 0; j <= i; ++j) {
             const float vval = in_cache ? to_f32(vc[(((size_t)b * H + hh) * t_max + min(n + j, t_max - 1)) * dh + e])
                                         : to_f32(vs[((((size_t)(b * C + c)) * H + hh) * Tb + j) * dh + e]);
@@ -835,7 +839,7 @@ void launch_attention(evs_handle* h, int li, const Pass& p) {
     int splits = g.kv_splits, chunk = g.kv_chunk;
     if (plan.ok && launch_attn_tc(h, li, p, plan)) {
         splits = plan.splits;
-        chunk = plan.tiles * 128;
+        chunk = 0;   // equal shares of the prefix over every split
     } else {
     dim3 grid(g.kv_splits, p.B * H, (Q + AQ - 1) / AQ);
     if (is_bf16(h))
