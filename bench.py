@@ -183,7 +183,7 @@ def traffic_per_round(wl, kind):
     """DRAM bytes one round's launches of a kernel kind moved in an ncu capture, as recorded
     in profiles/traffic.txt, if the kernel source is unchanged since (else None)."""
     import hashlib
-    src = {"gemm": "gemm_tc.cu", "attn": "attn_tc.cu"}.get(kind)
+    src = {"gemm": "gemm_tc.cu", "attn": "attn_fa.cu"}.get(kind)
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if src is None or not os.path.exists(path):
         return None

@@ -1,6 +1,6 @@
-// Split-KV attention over the readable KV prefix for many queries per sequence (17..128:
-// several candidates' blocks, prefill chunks), streamed through tcgen05 tensor cores with
-// an online softmax.
+// Split-KV attention over the readable KV prefix for up to 128 queries per sequence (every
+// block position of every candidate, or a prefill chunk), streamed through tcgen05 tensor
+// cores with an online softmax.
 //
 // One CTA per (prefix chunk, sequence x head); the chunks are equal shares of the key tiles
 // of the sequence's readable prefix, worked out from its length at run time. The queries
@@ -355,31 +355,52 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 }
 
 // ---- host side ------------------------------------------------------------------------------
-// Splits of a pass with Q (17..128) queries per sequence: chunks of at most 16 tiles, and as
-// many more splits (up to twice that) as make the grid fill whole waves of one CTA per SM.
-AttnPlan attn_fa_plan(int Q, int B, int H, int t_max, int smem_max) {
+static PFN_cuTensorMapEncodeTiled_v12000 kv_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+bool make_kv_map(CUtensorMap* m, const void* base, int t_max, int bh) {
+    auto fn = kv_encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)FA_DH, (cuuint64_t)t_max, (cuuint64_t)bh};
+    const cuuint64_t strides[2] = {(cuuint64_t)FA_DH * 2, (cuuint64_t)t_max * FA_DH * 2};
+    const cuuint32_t box[3] = {64, FA_KEYS, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Splits of a pass with Q (1..128) queries per sequence: the count that minimises waves of
+// one CTA per SM x (tiles per CTA + FA_CTA_OVERHEAD), the start-up and drain of a CTA costing
+// about that many tiles' streaming time.
+#ifndef FA_CTA_OVERHEAD
+#define FA_CTA_OVERHEAD 2
+#endif
+AttnPlan attn_plan(int Q, int B, int H, int t_max, int smem_max) {
     AttnPlan p{};
-    if (Q < 17 || Q > FA_ROWS) return p;
+    if (Q < 1 || Q > FA_ROWS) return p;
     const int fixed = 1024 + 3 * FA_TILE + 16 * 8;   // align, Q, two P buffers, barriers
     int stages = (smem_max - fixed) / FA_TILE;
     if (stages > 3) stages = 3;
     if (stages < 2) return p;
     const long long total_tiles = (t_max + FA_KEYS - 1) / FA_KEYS;
     const long long bh = (long long)B * H;
-    long long s_min = (total_tiles + 15) / 16;
-    if (s_min < 1) s_min = 1;
-    long long best = s_min;
-    if (bh * s_min < 152) {
-        best = 152 / bh > s_min ? 152 / bh : s_min;    // one partial wave: fill it
-    } else {
-        double best_eff = 0.0;
-        for (long long s = s_min; s <= 2 * s_min; ++s) {
-            const long long ctas = bh * s, waves = (ctas + 151) / 152;
-            const double eff = (double)ctas / (double)(waves * 152);
-            if (eff > best_eff + 1e-9) { best_eff = eff; best = s; }
-        }
+    long long best = 1, best_cost = -1;
+    for (long long s = 1; s <= total_tiles && s <= 4096; ++s) {
+        const long long waves = (bh * s + 151) / 152;
+        const long long cost = waves * ((total_tiles + s - 1) / s + FA_CTA_OVERHEAD);
+        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = s; }
     }
-    p.fa = 1;
     p.n_q = FA_ROWS;
     p.splits = (int)best;
     p.tiles = (int)((total_tiles + best - 1) / best);
@@ -390,7 +411,7 @@ AttnPlan attn_fa_plan(int Q, int B, int H, int t_max, int smem_max) {
     return p;
 }
 
-int attn_fa_init() {
+int attn_init() {
     int dev = 0, optin = 0;
     cudaFuncAttributes fa;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -403,7 +424,7 @@ int attn_fa_init() {
     return dyn;
 }
 
-bool launch_attn_fa(evs_handle* h, int li, const Pass& p, const AttnPlan& plan) {
+bool launch_attn_tensor(evs_handle* h, int li, const Pass& p, const AttnPlan& plan) {
     const LayerDesc& L = h->layer[li];
     const int H = L.param;
     CUtensorMap tk, tv;

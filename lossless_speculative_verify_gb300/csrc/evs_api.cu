@@ -194,8 +194,8 @@ size_t carve(const evs_config& c, char* base, evs_handle* h) {
     if (c.dtype == EVS_DTYPE_BF16 && c.head_dim == 128) {
         // the tensor-core attention may chunk the prefix more finely (its plan depends only
         // on the pass shape and t_max; 200 KiB stands in for the shared-memory limit here)
-        const evs::AttnPlan pv = evs::attn_tc_plan(g.C * g.T, g.B, g.h_max, c.t_max, 200 * 1024);
-        const evs::AttnPlan pp = evs::attn_tc_plan(c.prefill_chunk, g.B, g.h_max, c.t_max, 200 * 1024);
+        const evs::AttnPlan pv = evs::attn_plan(g.C * g.T, g.B, g.h_max, c.t_max, 200 * 1024);
+        const evs::AttnPlan pp = evs::attn_plan(c.prefill_chunk, g.B, g.h_max, c.t_max, 200 * 1024);
         splits_max = std::max(splits_max, (size_t)std::max(pv.splits, pp.splits));
     }
     char* part = take(B * (size_t)g.h_max * splits_max * g.q_max * (dh + 2) * 4);
@@ -361,7 +361,7 @@ evs_status evs_create(const evs_config* cfg, const evs_weights* weights, void* w
     h->fused = cfg->dtype == EVS_DTYPE_BF16 && cfg->d % 128 == 0 && cfg->vocab % 128 == 0 && h->g.M_max <= 512;
     if (cfg->dtype == EVS_DTYPE_BF16) {
         h->tc_smem_max = evs::gemm_tc_init();
-        const int attn_smem = std::min(evs::attn_tc_init(), evs::attn_fa_init());
+        const int attn_smem = evs::attn_init();
         if (h->tc_smem_max < 0 || attn_smem < 0) {
             free(h);
             return EVS_ERR_CUDA;
@@ -369,8 +369,8 @@ evs_status evs_create(const evs_config* cfg, const evs_weights* weights, void* w
         if (cfg->head_dim == 128) {
             // plans use at most 200 KiB, the bound the partial buffer was sized with
             const int sm = std::min(attn_smem, 200 * 1024);
-            h->plan_verify = evs::attn_tc_plan(h->g.C * h->g.T, h->g.B, h->g.h_max, cfg->t_max, sm);
-            h->plan_prefill = evs::attn_tc_plan(cfg->prefill_chunk, h->g.B, h->g.h_max, cfg->t_max, sm);
+            h->plan_verify = evs::attn_plan(h->g.C * h->g.T, h->g.B, h->g.h_max, cfg->t_max, sm);
+            h->plan_prefill = evs::attn_plan(cfg->prefill_chunk, h->g.B, h->g.h_max, cfg->t_max, sm);
         }
     }
     evs_status st = cuda_ok(cudaMemcpyAsync(h->layer_dev, h->layer, sizeof(evs::LayerDesc) * cfg->n_layers,

@@ -34,13 +34,12 @@ struct Geometry {
     int kv_splits;    // ceil(t_max / kv_chunk)
 };
 
-// Prefix chunking of the tensor-core attention for one pass shape (attn_tc.cu).
+// Prefix chunking of the tensor-core attention for one pass shape (attn_fa.cu).
 struct AttnPlan {
-    int ok;          // 1 if a tensor-core kernel takes this pass
-    int fa;          // 1: queries on the TMEM lanes, online softmax (attn_fa.cu)
-    int n_q;         // queries padded to 16 (MMA N)
-    int tiles;       // 128-key tiles per CTA
-    int splits;      // chunks covering t_max keys
+    int ok;          // 1 if the tensor-core kernel takes this pass
+    int n_q;         // query rows of the products (128, padded)
+    int tiles;       // most 128-key tiles a CTA streams
+    int splits;      // chunks of the prefix per sequence and head
     int stages;      // TMA ring depth (32 KiB stages)
     int ncols;       // TMEM columns
     int smem;        // dynamic shared memory bytes
@@ -129,13 +128,10 @@ void launch_gemm(evs_handle* h, const void* A, const void* W, float* Y, int M, i
 bool gemm_tc_supported(int M, int N, int K);
 int gemm_tc_init();
 int tc_cta_target();
-// tcgen05 attention (attn_tc.cu)
-AttnPlan attn_tc_plan(int Q, int B, int H, int t_max, int smem_max);
-int attn_tc_init();
-bool launch_attn_tc(evs_handle* h, int layer, const Pass& p, const AttnPlan& plan);
-AttnPlan attn_fa_plan(int Q, int B, int H, int t_max, int smem_max);
-int attn_fa_init();
-bool launch_attn_fa(evs_handle* h, int layer, const Pass& p, const AttnPlan& plan);
+// tcgen05 attention (attn_fa.cu)
+AttnPlan attn_plan(int Q, int B, int H, int t_max, int smem_max);
+int attn_init();
+bool launch_attn_tensor(evs_handle* h, int layer, const Pass& p, const AttnPlan& plan);
 // 3-D tensor map over a [bh][t_max][128] bf16 K or V cache, boxes of 128 rows x 64 columns
 bool make_kv_map(CUtensorMap* m, const void* base, int t_max, int bh);
 bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, float* Y, int M, int N,

@@ -837,7 +837,7 @@ void launch_attention(evs_handle* h, int li, const Pass& p) {
     const Geometry& g = h->g;
     const AttnPlan& plan = p.commit ? h->plan_prefill : h->plan_verify;
     int splits = g.kv_splits, chunk = g.kv_chunk;
-    if (plan.ok && launch_attn_tc(h, li, p, plan)) {
+    if (plan.ok && launch_attn_tensor(h, li, p, plan)) {
         splits = plan.splits;
         chunk = 0;   // equal shares of the prefix over every split
     } else {

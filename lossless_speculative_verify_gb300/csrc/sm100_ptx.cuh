@@ -92,14 +92,8 @@ __device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
     return r != 0;
 }
 
-// 2^x by the hardware approximation (MUFU); callers fold ln -> log2 scaling themselves.
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// As ex2_approx, flushing subnormal inputs and results to zero (one MUFU operation).
+// 2^x by the hardware approximation (MUFU), subnormal inputs and results flushed to zero;
+// callers fold ln -> log2 scaling themselves.
 __device__ __forceinline__ float ex2_approx_ftz(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
