@@ -347,87 +347,157 @@ __global__ void __launch_bounds__(256) attn_split_kernel(
 }
 
 // Merge the prefix partials with the in-block causal keys of the query's own candidate,
-// normalise, and store o in the projection dtype. One CTA per (sequence x head, query);
-// thread e owns output column e. Partials are fetched in parallel: first every split's
-// (m, l) by its own thread, then the in-block scores one warp per key, then o.
-constexpr int CMB_MAX_SPLITS = 1024;
+// normalise, and store o in the projection dtype. One CTA (four warps) per (sequence x head,
+// candidate, four consecutive block positions), a warp per query; lanes own dh/32 output
+// columns. The partials are folded in eight chunks at a time (every load of a batch in
+// flight before any is used) with a running maximum; then the in-block keys j <= i, staged
+// 32 rows at a time in shared memory, one score per lane, the same way. dh is 16..128.
+constexpr int CMB_ROWS = 32;
+constexpr int CMB_DHMAX = 128;
 
-template <typename T>
+template <typename T, int EPL>
 __global__ void __launch_bounds__(128, 4) attn_combine_kernel(
     const float* __restrict__ Y, int ldy, const T* __restrict__ kc, const T* __restrict__ vc,
     const T* __restrict__ ks, const T* __restrict__ vs, int H, int dh, int C, int Tb, int Q, int q_max,
     int t_max, int splits, int chunk, int in_cache, const int32_t* __restrict__ kv_base,
     const float* __restrict__ part, T* __restrict__ out, int d) {
-    pdl_trigger();
+    // dependents launch only once the attention partials are complete: an output projection
+    // starting earlier would stream its weights against the attention kernel's K / V reads
     pdl_wait();
-    __shared__ float w_s[CMB_MAX_SPLITS];
-    __shared__ float l_s[CMB_MAX_SPLITS];
-    __shared__ float sc_blk[128];
-    __shared__ float red[32];
-    const int bh = blockIdx.x, qi = blockIdx.y, b = bh / H, hh = bh % H;
-    const int c = qi / Tb, i = qi % Tb;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+    pdl_trigger();
+    // in-block rows in the cache dtype (small enough to share an SM with the attention
+    // kernel, so the launch can start early); key rows padded so one key per lane is
+    // conflict-free
+    __shared__ T k_s[CMB_ROWS][CMB_DHMAX + 2];
+    __shared__ __align__(16) T v_s[CMB_ROWS][CMB_DHMAX];
+    __shared__ float q_s[4][CMB_DHMAX];
+    const int bh = blockIdx.x, c = blockIdx.y, b = bh / H, hh = bh % H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int i0 = blockIdx.z * 4, i = i0 + warp;
+    const int i_end = min(i0 + 4, Tb);                   // queries of this CTA: [i0, i_end)
+    const bool live = i < Tb;
+    const int qi = c * Tb + i;
     const int n = kv_base[b];  // rows n + j past t_max were never written (overflow flag set);
                                // their reads are clamped to stay in bounds
-    // chunk > 0: fixed chunks, the first ceil(n / chunk) splits hold keys; chunk == 0: the
-    // prefix is shared out over every split (empty ones report m = -inf)
-    const int used = min(chunk > 0 ? min((n + chunk - 1) / chunk, splits) : splits, CMB_MAX_SPLITS);
-    const float* pbase = part + (((size_t)b * H + hh) * splits * q_max + qi) * (dh + 2);
-    const size_t pstride = (size_t)q_max * (dh + 2);
-    float M = -INFINITY;
-    for (int s = tid; s < used; s += blockDim.x) {
-        const float ms = pbase[s * pstride + dh];
-        w_s[s] = ms;
-        l_s[s] = pbase[s * pstride + dh + 1];
-        M = fmaxf(M, ms);
-    }
-    // in-block scores q . k_j / sqrt(dh), j = 0..i, one warp per key
+    const int used = chunk > 0 ? min((n + chunk - 1) / chunk, splits) : splits;
     const float scale = rsqrtf((float)dh);
-    const float* qrow = Y + ((size_t)b * Q + qi) * ldy + hh * dh;
-    for (int j = warp; j <= i; j += nw) {
-        const T* krow = in_cache ? kc + (((size_t)b * H + hh) * t_max + min(n + j, t_max - 1)) * dh
-                                 : ks + ((((size_t)(b * C + c)) * H + hh) * Tb + j) * dh;
-        float acc = 0.f;
-        for (int e = lane; e < dh; e += 32) acc = fmaf(qrow[e], to_f32(krow[e]), acc);
-        acc = warp_sum(acc) * scale;
-        if (lane == 0) sc_blk[j] = acc;
-    }
-    __syncthreads();
-    for (int j = tid; j <= i; j += blockDim.x) M = fmaxf(M, sc_blk[j]);
-    M = block_max(M, red);
-    float L = 0.f;
-    for (int s = tid; s < used; s += blockDim.x) {
-        const float ms = w_s[s];
-        const float w = (ms == -INFINITY) ? 0.f : __expf(ms - M);
-        w_s[s] = w;
-        L = fmaf(l_s[s], w, L);
-    }
-    for (int j = tid; j <= i; j += blockDim.x) {
-        const float w = __expf(sc_blk[j] - M);
-        sc_blk[j] = w;
-        L += w;
-    }
-    L = block_sum(L, red);   // also orders the w_s / sc_blk writes before the reads below
-    for (int e = tid; e < dh; e += blockDim.x) {
-        float O = 0.f;
-        int s = 0;
-        // splits of weight 0 (empty, or negligible) are skipped: an empty split leaves its o
-        // unwritten. Eight splits' loads in flight before any is summed.
-        for (; s + 8 <= used; s += 8) {
-            float a8[8];
+    const int e0 = lane * EPL;
+    const bool act = e0 < dh;
+    // issue the query row and the first in-block rows' loads together, then store them
+    float qv[CMB_DHMAX / 32];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) a8[u] = w_s[s + u] != 0.f ? pbase[(s + u) * pstride + e] : 0.f;
+    for (int u = 0; u < CMB_DHMAX / 32; ++u) {
+        const int e = lane + 32 * u;
+        qv[u] = (live && e < dh) ? Y[((size_t)b * Q + qi) * ldy + hh * dh + e] : 0.f;
+    }
+    constexpr int PE = 16 / sizeof(T);                   // elements per 16-byte piece
+    constexpr int MAXP = CMB_ROWS * CMB_DHMAX / PE / 128;
+    const int per_row = dh / PE;
+    uint4 kr4[MAXP], vr4[MAXP];
+    auto stage_load = [&](int j0, int jn) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) O = fmaf(a8[u], w_s[s + u], O);
+        for (int u = 0; u < MAXP; ++u) {
+            const int idx = tid + 128 * u;
+            if (idx < jn * per_row) {
+                const int jj = idx / per_row, e = (idx % per_row) * PE, j = j0 + jj;
+                const size_t kr = in_cache ? (((size_t)b * H + hh) * t_max + min(n + j, t_max - 1)) * dh
+                                           : ((((size_t)(b * C + c)) * H + hh) * Tb + j) * dh;
+                kr4[u] = *reinterpret_cast<const uint4*>((in_cache ? kc : ks) + kr + e);
+                vr4[u] = *reinterpret_cast<const uint4*>((in_cache ? vc : vs) + kr + e);
+            }
         }
-        for (; s < used; ++s)
-            if (w_s[s] != 0.f) O = fmaf(pbase[s * pstride + e], w_s[s], O);
-        for (int j = 0; j <= i; ++j) {
-            const float vval = in_cache ? to_f32(vc[(((size_t)b * H + hh) * t_max + min(n + j, t_max - 1)) * dh + e])
-                                        : to_f32(vs[((((size_t)(b * C + c)) * H + hh) * Tb + j) * dh + e]);
-            O = fmaf(sc_blk[j], vval, O);
+    };
+    auto stage_store = [&](int jn) {
+#pragma unroll
+        for (int u = 0; u < MAXP; ++u) {
+            const int idx = tid + 128 * u;
+            if (idx < jn * per_row) {
+                const int jj = idx / per_row, e = (idx % per_row) * PE;
+                const T* kp = reinterpret_cast<const T*>(&kr4[u]);
+#pragma unroll
+                for (int x = 0; x < PE; ++x) k_s[jj][e + x] = kp[x];
+                *reinterpret_cast<uint4*>(&v_s[jj][e]) = vr4[u];
+            }
         }
-        out[((size_t)b * Q + qi) * d + hh * dh + e] = from_f32<T>(O / L);
+    };
+    stage_load(0, min(CMB_ROWS, i_end));
+    float M = -INFINITY, L = 0.f, O[EPL];
+#pragma unroll
+    for (int u = 0; u < EPL; ++u) O[u] = 0.f;
+    // fold a batch with maximum mb: rescale what is summed when the running maximum moves
+    auto rebase = [&](float mb) {
+        if (mb > M) {
+            const float f = M == -INFINITY ? 0.f : __expf(M - mb);
+            L *= f;
+#pragma unroll
+            for (int u = 0; u < EPL; ++u) O[u] *= f;
+            M = mb;
+        }
+    };
+    if (live) {
+        const float* pq = part + ((size_t)bh * splits * q_max + qi) * (dh + 2);
+        const size_t pstride = (size_t)q_max * (dh + 2);
+        for (int s0 = 0; s0 < used; s0 += 8) {
+            float ms[8], ls[8], os[8][EPL];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const bool on = s0 + j < used;
+                ms[j] = on ? pq[(s0 + j) * pstride + dh] : -INFINITY;
+                ls[j] = on ? pq[(s0 + j) * pstride + dh + 1] : 0.f;
+#pragma unroll
+                for (int u = 0; u < EPL; ++u) os[j][u] = (on && act) ? pq[(s0 + j) * pstride + e0 + u] : 0.f;
+            }
+            float mb = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) mb = fmaxf(mb, ms[j]);
+            if (mb == -INFINITY) continue;        // empty chunks only
+            rebase(mb);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (ms[j] == -INFINITY) continue;  // an empty chunk leaves its o unwritten
+                const float w = __expf(ms[j] - M);
+                L = fmaf(ls[j], w, L);
+#pragma unroll
+                for (int u = 0; u < EPL; ++u) O[u] = fmaf(os[j][u], w, O[u]);
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < CMB_DHMAX / 32; ++u)
+        if (lane + 32 * u < dh) q_s[warp][lane + 32 * u] = qv[u];
+    stage_store(min(CMB_ROWS, i_end));
+    // in-block keys j <= i, 32 staged rows at a time (the CTA's queries see keys < i_end);
+    // the first rows were staged above
+    for (int j0 = 0; j0 < i_end; j0 += CMB_ROWS) {
+        const int jn = min(CMB_ROWS, i_end - j0);
+        if (j0 > 0) {
+            __syncthreads();                      // the previous rows are no longer read
+            stage_load(j0, jn);
+            stage_store(jn);
+        }
+        __syncthreads();
+        if (!live || j0 > i) continue;
+        const int jhi = min(jn - 1, i - j0);      // last staged key this query sees
+        float sc = -INFINITY;
+        if (lane <= jhi) {
+            float acc = 0.f;
+            for (int e = 0; e < dh; ++e) acc = fmaf(q_s[warp][e], to_f32(k_s[lane][e]), acc);
+            sc = acc * scale;
+        }
+        rebase(warp_max(sc));
+        const float w = lane <= jhi ? __expf(sc - M) : 0.f;
+        L += warp_sum(w);
+        for (int jj = 0; jj <= jhi; ++jj) {
+            const float wj = __shfl_sync(0xffffffffu, w, jj);
+#pragma unroll
+            for (int u = 0; u < EPL; ++u)
+                if (act) O[u] = fmaf(wj, to_f32(v_s[jj][e0 + u]), O[u]);
+        }
+    }
+    if (live && act) {
+        const float inv = 1.f / L;
+#pragma unroll
+        for (int u = 0; u < EPL; ++u) out[((size_t)b * Q + qi) * d + hh * dh + e0 + u] = from_f32<T>(O[u] * inv);
     }
 }
 
@@ -853,16 +923,17 @@ void launch_attention(evs_handle* h, int li, const Pass& p) {
     h->launches++;
     prof_end(h, EVS_K_ATTN);
     prof_begin(h, EVS_K_ATTN_COMBINE);
-    dim3 grid2(p.B * H, Q);
-    const int thr = 128;
-    if (is_bf16(h))
-        launch_k(h, attn_combine_kernel<bf16>, dim3(grid2), dim3(thr), 0, h->y, 3 * d, (const bf16*)L.kc,
-            (const bf16*)L.vc, (const bf16*)L.ks, (const bf16*)L.vs, H, dh, p.C, p.T, Q, g.q_max, h->cfg.t_max,
-            splits, chunk, p.kv_in_cache, h->kv_base, h->attn_part, (bf16*)h->act, d);
-    else
-        launch_k(h, attn_combine_kernel<float>, dim3(grid2), dim3(thr), 0, h->y, 3 * d, (const float*)L.kc,
-            (const float*)L.vc, (const float*)L.ks, (const float*)L.vs, H, dh, p.C, p.T, Q, g.q_max,
-            h->cfg.t_max, splits, chunk, p.kv_in_cache, h->kv_base, h->attn_part, (float*)h->act, d);
+    dim3 grid2(p.B * H, p.C, (p.T + 3) / 4);
+#define EVS_CMB(TY, EPL)                                                                                \
+    launch_k(h, attn_combine_kernel<TY, EPL>, dim3(grid2), dim3(128), 0, h->y, 3 * d, (const TY*)L.kc,       \
+             (const TY*)L.vc, (const TY*)L.ks, (const TY*)L.vs, H, dh, p.C, p.T, Q, g.q_max, h->cfg.t_max, \
+             splits, chunk, p.kv_in_cache, h->kv_base, h->attn_part, (TY*)h->act, d)
+    if (is_bf16(h)) {
+        if (dh > 64) EVS_CMB(bf16, 4); else if (dh > 32) EVS_CMB(bf16, 2); else EVS_CMB(bf16, 1);
+    } else {
+        if (dh > 64) EVS_CMB(float, 4); else if (dh > 32) EVS_CMB(float, 2); else EVS_CMB(float, 1);
+    }
+#undef EVS_CMB
     h->launches++;
     prof_end(h, EVS_K_ATTN_COMBINE);
 }
