@@ -43,6 +43,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-also", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--prefix", type=int, default=None,
+                    help="cached tokens per sequence instead of the workload's (small profiling "
+                         "cases; the workload name then carries the override)")
     return ap.parse_args()
 
 
@@ -367,6 +370,8 @@ def main():
     args = parse()
     from synth import get_workload
     wl = get_workload(args.workload)
+    if args.prefix is not None:
+        wl = wl.replace(prefix_len=args.prefix, name=f"{wl.name}@prefix{args.prefix}")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
