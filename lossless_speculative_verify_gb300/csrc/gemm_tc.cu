@@ -215,17 +215,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int mc_lo = (int)(128LL * split / p.splits);
     const int mcw = (int)(128LL * (split + 1) / p.splits) - mc_lo;
     const int mT = p.mix_T > 0 ? p.mix_T : 1, mgroups = p.M / mT;
-    // FIR item: one (sequence-candidate g, channel) pair; taps w[j] and the history
-    // prev[j] = x_{-1-j} (the newest carried input first), zero past the filter length
-    auto fir_load = [&](int pair, float (&w)[16], float (&prev)[15]) {
+    // FIR item: one (group g, block position t, channel c), channels fastest: its taps w[j],
+    // zero past the filter length
+    auto fir_load = [&](int item, float (&w)[16]) {
         const int L = p.mix_param;
-        const bool on = pair < mgroups * mcw;
-        const int g = on ? pair / mcw : 0, n = n0 + mc_lo + (on ? pair % mcw : 0), b = g / p.mix_C;
+        const bool on = item < mgroups * mT * mcw;
+        const int n = n0 + mc_lo + (on ? item % mcw : 0);
 #pragma unroll
         for (int j = 0; j < 16; ++j) w[j] = (on && j < L) ? p.taps[(size_t)n * L + j] : 0.f;
-#pragma unroll
-        for (int j = 0; j < 15; ++j)
-            prev[j] = (on && j < L - 1) ? p.tail[((size_t)b * (L - 1) + (L - 2 - j)) * p.d + n] : 0.f;
     };
     // IIR item: one (g, channel, pole); pole lambda, input weight B, readout weight C, state
     auto iir_load = [&](int it, float2& l, float2& bq, float2& cq, float2& sv) {
@@ -239,10 +236,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             sv = p.state[((size_t)b * p.d + n) * N + k];
         }
     };
-    float fw[16], fprev[15];
+    float fw[16];
     float2 il0, ib0, ic0, is0, il1, ib1, ic1, is1;
     if (p.mix == 1) {
-        fir_load(threadIdx.x, fw, fprev);
+        fir_load(threadIdx.x, fw);
     } else if (p.mix == 2) {
         iir_load(threadIdx.x, il0, ib0, ic0, is0);
         iir_load(threadIdx.x + blockDim.x, il1, ib1, ic1, is1);
@@ -427,81 +424,153 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int vld = S == 1 ? TC_BM : cw;      // row stride of vals
         const int T = p.mix_T, groups = p.M / T;
         const int voff = S == 1 ? c_lo : 0;       // column of this CTA's first channel in vals
-        if (p.mix == 1 && !bad) {
-            // FIR: one thread per (sequence-candidate, channel), y_t = sum_j w_j x_{t-j}
+        // the mixer's input x_t of block row (g, t), channel column c of vals (1/rms applied)
+        auto xin = [&](int g, int t, int c) -> float {
+            return vals[(size_t)(g * T + t) * vld + voff + c] * (p.ssq_in ? rinv_s[g * T + t] : 1.f);
+        };
+        if (p.mix == 1) {
+            // FIR, y_t = sum_j w_j x_{t-j}: no recurrence, so one thread per (group, block
+            // position, channel), channels fastest (coalesced stores); x_{-m} for m >= 1 is
+            // row L-1-m of the carried tail
             const int L = p.mix_param;
-            for (int pair = threadIdx.x; pair < groups * cw; pair += blockDim.x) {
-                if (pair != (int)threadIdx.x) fir_load(pair, fw, fprev);
-                const int g = pair / cw, c = pair % cw, n = n0 + c_lo + c, b = g / p.mix_C;
-                const float* vrow = vals + (size_t)g * T * vld + voff + c;
-                float* st = p.stage + (size_t)g * (L - 1 + T) * p.d;
-                if (!p.mix_commit) {
+            const int items = groups * T * cw;
+            for (int it = threadIdx.x; it < items && !bad; it += blockDim.x) {
+                if (it != (int)threadIdx.x && blockDim.x % cw != 0) fir_load(it, fw);   // else same channel
+                const int c = it % cw, t = (it / cw) % T, g = it / (cw * T);
+                const int n = n0 + c_lo + c, b = g / p.mix_C;
+                const float* tl = p.tail + (size_t)b * (L - 1) * p.d + n;
+                float xv[16];   // x_{t-j}: every input's load issued before the sum
 #pragma unroll
-                    for (int j = 0; j < 15; ++j)
-                        if (j < L - 1) st[(size_t)(L - 2 - j) * p.d + n] = fprev[j];
+                for (int j = 0; j < 16; ++j)
+                    xv[j] = j >= L ? 0.f : (t - j >= 0 ? xin(g, t - j, c) : tl[(size_t)(L - 1 - j + t) * p.d]);
+                float y = fw[0] * xv[0];
+#pragma unroll
+                for (int j = 1; j < 16; ++j)
+                    if (j < L) y = fmaf(fw[j], xv[j], y);
+                p.mix_out[((size_t)g * T + t) * p.d + n] = __float2bfloat16_rn(y);
+                if (!p.mix_commit) {   // stage rows [tail || block inputs] of this group
+                    float* st = p.stage + (size_t)g * (L - 1 + T) * p.d + n;
+                    st[(size_t)(L - 1 + t) * p.d] = xv[0];
+                    if (t == 0) {   // every row's load issued before any store
+                        float tv[15];
+#pragma unroll
+                        for (int r = 0; r < 15; ++r) tv[r] = r < L - 1 ? tl[(size_t)r * p.d] : 0.f;
+#pragma unroll
+                        for (int r = 0; r < 15; ++r)
+                            if (r < L - 1) st[(size_t)r * p.d] = tv[r];
+                    }
                 }
-                for (int t = 0; t < T; ++t) {
-                    const float v = vrow[(size_t)t * vld] * (p.ssq_in ? rinv_s[g * T + t] : 1.f);
-                    float y = fw[0] * v;
+            }
+            if (p.mix_commit && L > 1) {
+                // new tail rows i = x_{T-(L-1)+i} (row i+T of the old tail while that is
+                // negative). Items (sequence, row, channel) in rounds; a round reads all its
+                // values before writing any, and the old rows it reads are written only by
+                // the same or a later round (rows ascend with the item index).
+                const int tail_items = (groups / p.mix_C) * (L - 1) * cw;   // one per sequence
+                for (int r0 = 0; r0 < tail_items; r0 += 4 * (int)blockDim.x) {
+                    float nv[4];
 #pragma unroll
-                    for (int j = 1; j < 16; ++j)
-                        if (j < L) y = fmaf(fw[j], fprev[j - 1], y);
+                    for (int u = 0; u < 4; ++u) {
+                        const int it = r0 + threadIdx.x + u * blockDim.x;
+                        nv[u] = 0.f;
+                        if (it < tail_items) {
+                            const int c = it % cw, i = (it / cw) % (L - 1), bq = it / (cw * (L - 1));
+                            const int g = bq * p.mix_C, t = T - (L - 1) + i, n = n0 + c_lo + c;
+                            nv[u] = t >= 0 ? xin(g, t, c) : p.tail[((size_t)bq * (L - 1) + (i + T)) * p.d + n];
+                        }
+                    }
+                    __syncthreads();
 #pragma unroll
-                    for (int j = 14; j > 0; --j) fprev[j] = fprev[j - 1];
-                    fprev[0] = v;
-                    p.mix_out[((size_t)g * T + t) * p.d + n] = __float2bfloat16_rn(y);
-                    if (!p.mix_commit) st[(size_t)(L - 1 + t) * p.d + n] = v;
-                }
-                if (p.mix_commit) {
-#pragma unroll
-                    for (int j = 0; j < 15; ++j)
-                        if (j < L - 1) p.tail[((size_t)b * (L - 1) + (L - 2 - j)) * p.d + n] = fprev[j];
+                    for (int u = 0; u < 4; ++u) {
+                        const int it = r0 + threadIdx.x + u * blockDim.x;
+                        if (it < tail_items && !bad) {
+                            const int c = it % cw, i = (it / cw) % (L - 1), bq = it / (cw * (L - 1));
+                            p.tail[((size_t)bq * (L - 1) + i) * p.d + n0 + c_lo + c] = nv[u];
+                        }
+                    }
+                    __syncthreads();
                 }
             }
         } else if (p.mix == 2) {
-            // modal IIR: N consecutive lanes hold the N poles of one channel (N divides 32),
-            // the readout summed by a shuffle reduction over them; two items per thread at a
-            // time (it and it + blockDim.x), their recurrences interleaved
+            // modal IIR: items (group, channel, pole), two per thread per round, their
+            // recurrences interleaved. The serial loop keeps only the state update; the
+            // per-pole readouts and (verify) the states go to shared memory, and after the
+            // loop a thread per (group, position, channel) sums the readout over the poles
+            // and the retained states are copied out with coalesced stores.
             const int N = p.mix_param;
-            const int items = groups * cw * N;                    // (group, channel, pole)
-            const int span = (items + 31) / 32 * 32;              // whole warps take part
-            const int nt = blockDim.x;
-            for (int it = threadIdx.x; it < span; it += 2 * nt) {
-                if (it != (int)threadIdx.x) {
-                    iir_load(it, il0, ib0, ic0, is0);
-                    iir_load(it + nt, il1, ib1, ic1, is1);
+            const int items = groups * cw * N;
+            const int nt = blockDim.x, round_items = 2 * nt;
+            // buffers after the partials and vals, 16-byte aligned: [T][round_items] each
+            const size_t used_f = S == 1 ? (size_t)p.M * TC_BM : (size_t)S * p.M * cwm + (size_t)p.M * cw;
+            float* qbuf = park + (used_f + 3) / 4 * 4;
+            float2* sbuf = reinterpret_cast<float2*>(qbuf + (size_t)T * round_items);
+            for (int base = 0; base < items; base += round_items) {
+                const int it0 = base + threadIdx.x, it1 = it0 + nt;
+                if (base > 0) {
+                    iir_load(it0, il0, ib0, ic0, is0);
+                    iir_load(it1, il1, ib1, ic1, is1);
+                    __syncthreads();                  // the previous round's buffers are read
                 }
-                const bool on0 = it < items && !bad, on1 = it + nt < items && !bad;
-                const int k0 = it % N, c0 = (it / N) % cw, g0 = min(it / (N * cw), groups - 1);
-                const int k1 = (it + nt) % N, c1 = ((it + nt) / N) % cw, g1 = min((it + nt) / (N * cw), groups - 1);
-                const int n_0 = n0 + c_lo + c0, n_1 = n0 + c_lo + c1;
-                const float* vr0 = vals + (size_t)g0 * T * vld + voff + c0;
-                const float* vr1 = vals + (size_t)g1 * T * vld + voff + c1;
+                const bool on0 = it0 < items && !bad, on1 = it1 < items && !bad;
+                const int c0 = (it0 / N) % cw, g0 = min(it0 / (N * cw), groups - 1);
+                const int c1 = (it1 / N) % cw, g1 = min(it1 / (N * cw), groups - 1);
+                const float* v0 = vals + (size_t)g0 * T * vld + voff + c0;
+                const float* v1 = vals + (size_t)g1 * T * vld + voff + c1;
+                const float* r0 = rinv_s + g0 * T;
+                const float* r1 = rinv_s + g1 * T;
+                float* q = qbuf + threadIdx.x;
+                float2* sv = sbuf + threadIdx.x;
                 for (int t = 0; t < T; ++t) {
-                    const float u0 = on0 ? vr0[(size_t)t * vld] * (p.ssq_in ? rinv_s[g0 * T + t] : 1.f) : 0.f;
-                    const float u1 = on1 ? vr1[(size_t)t * vld] * (p.ssq_in ? rinv_s[g1 * T + t] : 1.f) : 0.f;
+                    float u0 = on0 ? v0[(size_t)t * vld] : 0.f, u1 = on1 ? v1[(size_t)t * vld] : 0.f;
+                    if (p.ssq_in) {
+                        u0 *= r0[t];
+                        u1 *= r1[t];
+                    }
                     is0 = make_float2(fmaf(il0.x, is0.x, fmaf(-il0.y, is0.y, ib0.x * u0)),
                                       fmaf(il0.x, is0.y, fmaf(il0.y, is0.x, ib0.y * u0)));
                     is1 = make_float2(fmaf(il1.x, is1.x, fmaf(-il1.y, is1.y, ib1.x * u1)),
                                       fmaf(il1.x, is1.y, fmaf(il1.y, is1.x, ib1.y * u1)));
-                    float q0 = fmaf(ic0.x, is0.x, -ic0.y * is0.y);
-                    float q1 = fmaf(ic1.x, is1.x, -ic1.y * is1.y);
-                    for (int o = N >> 1; o > 0; o >>= 1) {
-                        q0 += __shfl_xor_sync(0xffffffffu, q0, o);
-                        q1 += __shfl_xor_sync(0xffffffffu, q1, o);
-                    }
-                    if (on0) {
-                        if (k0 == 0) p.mix_out[((size_t)g0 * T + t) * p.d + n_0] = __float2bfloat16_rn(q0);
-                        if (!p.mix_commit) p.ret[(((size_t)g0 * T + t) * p.d + n_0) * N + k0] = is0;
-                    }
-                    if (on1) {
-                        if (k1 == 0) p.mix_out[((size_t)g1 * T + t) * p.d + n_1] = __float2bfloat16_rn(q1);
-                        if (!p.mix_commit) p.ret[(((size_t)g1 * T + t) * p.d + n_1) * N + k1] = is1;
+                    q[(size_t)t * round_items] = fmaf(ic0.x, is0.x, -ic0.y * is0.y);
+                    q[(size_t)t * round_items + nt] = fmaf(ic1.x, is1.x, -ic1.y * is1.y);
+                    if (!p.mix_commit) {
+                        sv[(size_t)t * round_items] = is0;
+                        sv[(size_t)t * round_items + nt] = is1;
                     }
                 }
                 if (p.mix_commit) {
-                    if (on0) p.state[((size_t)(g0 / p.mix_C) * p.d + n_0) * N + k0] = is0;
-                    if (on1) p.state[((size_t)(g1 / p.mix_C) * p.d + n_1) * N + k1] = is1;
+                    const int k0 = it0 % N, k1 = it1 % N;
+                    if (on0) p.state[((size_t)(g0 / p.mix_C) * p.d + n0 + c_lo + c0) * N + k0] = is0;
+                    if (on1) p.state[((size_t)(g1 / p.mix_C) * p.d + n0 + c_lo + c1) * N + k1] = is1;
+                }
+                __syncthreads();
+                if (!bad) {
+                    // readout: the round's (group, channel) pairs (256 / N of them, a power of
+                    // two dividing the 128 threads); thread = pair, positions strided
+                    const int pairs = round_items / N, pl = threadIdx.x % pairs;
+                    const int pr = base / N + pl;
+                    if (pr * N < items) {
+                        const int c = pr % cw, g = pr / cw;
+                        __nv_bfloat16* yo = p.mix_out + (size_t)g * T * p.d + n0 + c_lo + c;
+                        for (int t = threadIdx.x / pairs; t < T; t += nt / pairs) {
+                            const float* qq = qbuf + (size_t)t * round_items + pl * N;
+                            float y = 0.f;
+                            for (int k = 0; k < N; ++k) y += qq[k];
+                            yo[(size_t)t * p.d] = __float2bfloat16_rn(y);
+                        }
+                    }
+                    if (!p.mix_commit) {
+                        // retained states [g][t][d][N]: this thread's two items, every position;
+                        // a warp's items are contiguous in the buffer and in memory
+                        const size_t tstride = (size_t)p.d * N;
+                        if (on0)
+                            for (int t = 0; t < T; ++t)
+                                p.ret[((size_t)g0 * T * p.d + n0 + c_lo + c0) * N + it0 % N + t * tstride] =
+                                    sbuf[(size_t)t * round_items + threadIdx.x];
+                        if (on1)
+                            for (int t = 0; t < T; ++t)
+                                p.ret[((size_t)g1 * T * p.d + n0 + c_lo + c1) * N + it1 % N + t * tstride] =
+                                    sbuf[(size_t)t * round_items + nt + threadIdx.x];
+                    }
                 }
             }
         }
@@ -776,9 +845,11 @@ bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, flo
             const LayerDesc& L = h->layer[fz->mix_layer];
             const evs_layer_weights& LW = h->w.layer[fz->mix_layer];
             const int cw = (TC_BM + t.splits - 1) / t.splits;
-            const size_t need = t.splits > 1 ? (size_t)(t.splits + 1) * M * cw * 4 : (size_t)M * TC_BM * 4;
+            size_t need = t.splits > 1 ? (size_t)(t.splits + 1) * M * cw * 4 : (size_t)M * TC_BM * 4;
+            if (L.kind == EVS_LAYER_IIR)   // readout and state buffers of one round (2 x 128 items)
+                need = (need + 15) / 16 * 16 + (size_t)ps->T * 256 * 12;
             const bool shape_ok = (t.splits == 1 || t.cluster) && need <= ring && M % ps->T == 0 &&
-                                  (L.kind == EVS_LAYER_FIR || 32 % L.param == 0);
+                                  (L.kind == EVS_LAYER_FIR || (32 % L.param == 0 && L.param >= 2));
             if (shape_ok) {
                 a.mix = L.kind == EVS_LAYER_FIR ? 1 : 2;
                 a.mix_C = ps->C;
