@@ -125,16 +125,19 @@ __global__ void fir_kernel(const float* __restrict__ Y, int ldy, T* __restrict__
     const int ch = blockIdx.x * blockDim.x + threadIdx.x;
     const int bc = blockIdx.y, b = bc / C;
     if (ch >= d) return;
-    float w[16], hist[16];
+    // w[j] taps; hist[j] = x_{t-1-j}, the newest input first (fixed register indices)
+    float w[16], hist[15];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        w[j] = (j < L) ? taps[(size_t)ch * L + j] : 0.f;
-        hist[j] = (j < L - 1) ? tail[((size_t)b * (L - 1) + j) * d + ch] : 0.f;
-    }
+    for (int j = 0; j < 16; ++j) w[j] = (j < L) ? taps[(size_t)ch * L + j] : 0.f;
+#pragma unroll
+    for (int j = 0; j < 15; ++j) hist[j] = (j < L - 1) ? tail[((size_t)b * (L - 1) + (L - 2 - j)) * d + ch] : 0.f;
     const int srows = L - 1 + Tb;
     float* st = stage + (size_t)bc * srows * d;
-    if (!commit)
-        for (int j = 0; j < L - 1; ++j) st[(size_t)j * d + ch] = hist[j];
+    if (!commit) {
+#pragma unroll
+        for (int j = 0; j < 15; ++j)
+            if (j < L - 1) st[(size_t)(L - 2 - j) * d + ch] = hist[j];
+    }
     for (int i0 = 0; i0 < Tb; i0 += 8) {
         float vin[8];   // eight positions' inputs requested before any is used
 #pragma unroll
@@ -143,24 +146,26 @@ __global__ void fir_kernel(const float* __restrict__ Y, int ldy, T* __restrict__
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int i = i0 + u;
-            if (i >= Tb) break;
-            const size_t m = (size_t)bc * Tb + i;
-            const float v = vin[u];
-            float y = w[0] * v;
-            // hist[L-2] = v_{t-1}, ..., hist[0] = v_{t-L+1}
+            if (i < Tb) {
+                const size_t m = (size_t)bc * Tb + i;
+                const float v = vin[u];
+                float y = w[0] * v;
 #pragma unroll
-            for (int j = 1; j < 16; ++j)
-                if (j < L) y = fmaf(w[j], hist[L - 1 - j], y);
+                for (int j = 1; j < 16; ++j)
+                    if (j < L) y = fmaf(w[j], hist[j - 1], y);
 #pragma unroll
-            for (int j = 0; j < 15; ++j)
-                if (j < L - 2) hist[j] = hist[j + 1];
-            hist[L - 2] = v;
-            out[m * d + ch] = from_f32<T>(y);
-            if (!commit) st[(size_t)(L - 1 + i) * d + ch] = v;
+                for (int j = 14; j > 0; --j) hist[j] = hist[j - 1];
+                hist[0] = v;
+                out[m * d + ch] = from_f32<T>(y);
+                if (!commit) st[(size_t)(L - 1 + i) * d + ch] = v;
+            }
         }
     }
-    if (commit)
-        for (int j = 0; j < L - 1; ++j) tail[((size_t)b * (L - 1) + j) * d + ch] = hist[j];
+    if (commit) {
+#pragma unroll
+        for (int j = 0; j < 15; ++j)
+            if (j < L - 1) tail[((size_t)b * (L - 1) + (L - 2 - j)) * d + ch] = hist[j];
+    }
 }
 
 // =========================================================================================
@@ -169,36 +174,50 @@ __global__ void fir_kernel(const float* __restrict__ Y, int ldy, T* __restrict__
 // Every s_t goes to the retained-state buffer (verify), or the last one to the state
 // (prefill).
 // =========================================================================================
-template <typename T>
-__global__ void iir_kernel(const float* __restrict__ Y, int ldy, T* __restrict__ out, int d,
-                           int N, int C, int Tb, int commit, const float2* __restrict__ lam,
-                           const float2* __restrict__ bb, const float2* __restrict__ cc,
-                           float2* __restrict__ state, float2* __restrict__ ret) {
+template <typename T, int NP>   // NP: poles per channel when fixed at compile time, else 0
+__global__ void __launch_bounds__(256) iir_kernel(const float* __restrict__ Y, int ldy, T* __restrict__ out, int d,
+                                                  int Nrt, int C, int Tb, int commit, const float2* __restrict__ lam,
+                                                  const float2* __restrict__ bb, const float2* __restrict__ cc,
+                                                  float2* __restrict__ state, float2* __restrict__ ret) {
     pdl_trigger();
     pdl_wait();
+    const int N = NP > 0 ? NP : Nrt;
     const int g = blockIdx.x * blockDim.x + threadIdx.x;
     const int bc = blockIdx.y, b = bc / C;
     if (g >= d * N) return;  // d*N is a multiple of 32: whole warps leave together
     const int ch = g / N, n = g % N;
     const float2 l = lam[g], bq = bb[g], cq = cc[g];
     float2 s = state[(size_t)b * d * N + g];
+    const float* yin = Y + (size_t)bc * Tb * ldy + ch;
+    float2* rp = ret + (size_t)bc * Tb * d * N + g;
+    T* op = out + (size_t)bc * Tb * d + ch;
+    const size_t rstride = (size_t)d * N;
     for (int i0 = 0; i0 < Tb; i0 += 8) {
-        float uin[8];   // eight positions' inputs requested before any is used
+        // eight positions: inputs requested together, the recurrence, then the eight
+        // readouts reduced over the pole lanes side by side
+        float uin[8], q[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) uin[k] = (i0 + k < Tb) ? Y[((size_t)bc * Tb + i0 + k) * ldy + ch] : 0.f;
+        for (int k = 0; k < 8; ++k) uin[k] = (i0 + k < Tb) ? yin[(size_t)(i0 + k) * ldy] : 0.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const int i = i0 + k;
-            if (i >= Tb) break;
-            const size_t m = (size_t)bc * Tb + i;
-            const float u = uin[k];
-            const float sx = fmaf(l.x, s.x, fmaf(-l.y, s.y, bq.x * u));
-            const float sy = fmaf(l.x, s.y, fmaf(l.y, s.x, bq.y * u));
-            s = make_float2(sx, sy);
-            float part = fmaf(cq.x, s.x, -cq.y * s.y);
-            for (int o = N >> 1; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-            if (n == 0) out[m * d + ch] = from_f32<T>(part);
-            if (!commit) ret[((size_t)bc * Tb + i) * d * N + g] = s;
+            if (i0 + k < Tb) {
+                const float u = uin[k];
+                s = make_float2(fmaf(l.x, s.x, fmaf(-l.y, s.y, bq.x * u)), fmaf(l.x, s.y, fmaf(l.y, s.x, bq.y * u)));
+                if (!commit) rp[(size_t)(i0 + k) * rstride] = s;
+            }
+            q[k] = fmaf(cq.x, s.x, -cq.y * s.y);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            if (o < N) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) q[k] += __shfl_xor_sync(0xffffffffu, q[k], o);
+            }
+        }
+        if (n == 0) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (i0 + k < Tb) op[(size_t)(i0 + k) * d] = from_f32<T>(q[k]);
         }
     }
     if (commit) state[(size_t)b * d * N + g] = s;
@@ -851,8 +870,8 @@ void launch_fir(evs_handle* h, int li, const Pass& p) {
     prof_begin(h, EVS_K_FIR);
     const int d = h->cfg.d;
     const LayerDesc& L = h->layer[li];
-    dim3 grid((d + 63) / 64, p.B * p.C);
     const float* taps = h->w.layer[li].fir_taps;
+    dim3 grid((d + 63) / 64, p.B * p.C);
     if (is_bf16(h))
         launch_k(h, fir_kernel<bf16>, dim3(grid), dim3(64), 0, h->y, 3 * d, (bf16*)h->act, d, p.C, p.T, p.commit, taps,
                                                        L.param, L.tail, L.stage);
@@ -872,12 +891,15 @@ void launch_iir(evs_handle* h, int li, const Pass& p) {
     const float2* lam = (const float2*)h->w.layer[li].iir_lambda;
     const float2* bb = (const float2*)h->w.layer[li].iir_b;
     const float2* cc = (const float2*)h->w.layer[li].iir_c;
-    if (is_bf16(h))
-        launch_k(h, iir_kernel<bf16>, dim3(grid), dim3(256), 0, h->y, 3 * d, (bf16*)h->act, d, N, p.C, p.T, p.commit,
-                                                       lam, bb, cc, L.state, L.ret);
-    else
-        launch_k(h, iir_kernel<float>, dim3(grid), dim3(256), 0, h->y, 3 * d, (float*)h->act, d, N, p.C, p.T, p.commit,
-                                                        lam, bb, cc, L.state, L.ret);
+#define EVS_IIR(TY, NP)                                                                                       \
+    launch_k(h, iir_kernel<TY, NP>, dim3(grid), dim3(256), 0, h->y, 3 * d, (TY*)h->act, d, N, p.C, p.T, p.commit, \
+             lam, bb, cc, L.state, L.ret)
+    if (is_bf16(h)) {
+        if (N == 16) EVS_IIR(bf16, 16); else EVS_IIR(bf16, 0);
+    } else {
+        if (N == 16) EVS_IIR(float, 16); else EVS_IIR(float, 0);
+    }
+#undef EVS_IIR
     h->launches++;
     prof_end(h, EVS_K_IIR);
 }
