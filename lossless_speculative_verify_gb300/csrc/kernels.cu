@@ -223,6 +223,75 @@ __global__ void __launch_bounds__(256) iir_kernel(const float* __restrict__ Y, i
     if (commit) state[(size_t)b * d * N + g] = s;
 }
 
+// The same scan with four poles per thread (N/4 lanes per channel): the readout needs only
+// log2(N/4) shuffle levels, and a thread's four retained states of a position are one
+// 32-byte run, so a warp writes eight channels' states as one contiguous kilobyte.
+template <typename T, int NP>
+__global__ void __launch_bounds__(256) iir_quad_kernel(const float* __restrict__ Y, int ldy, T* __restrict__ out,
+                                                       int d, int C, int Tb, int commit,
+                                                       const float2* __restrict__ lam, const float2* __restrict__ bb,
+                                                       const float2* __restrict__ cc, float2* __restrict__ state,
+                                                       float2* __restrict__ ret) {
+    constexpr int PPT = NP < 4 ? NP : 4;     // poles per thread
+    constexpr int LPC = NP / PPT;            // lanes per channel
+    pdl_trigger();
+    pdl_wait();
+    const int g = blockIdx.x * blockDim.x + threadIdx.x;
+    const int bc = blockIdx.y, b = bc / C;
+    if (g >= d * LPC) return;   // d*LPC is a multiple of 32 here: whole warps leave together
+    const int ch = g / LPC, k0 = (g % LPC) * PPT;
+    float2 l[PPT], bq[PPT], cq[PPT], s[PPT];
+#pragma unroll
+    for (int k = 0; k < PPT; ++k) {
+        l[k] = lam[(size_t)ch * NP + k0 + k];
+        bq[k] = bb[(size_t)ch * NP + k0 + k];
+        cq[k] = cc[(size_t)ch * NP + k0 + k];
+        s[k] = state[((size_t)b * d + ch) * NP + k0 + k];
+    }
+    const float* yin = Y + (size_t)bc * Tb * ldy + ch;
+    for (int i0 = 0; i0 < Tb; i0 += 8) {
+        float uin[8], q[8];   // eight positions' inputs requested before any is used
+#pragma unroll
+        for (int u = 0; u < 8; ++u) uin[u] = (i0 + u < Tb) ? yin[(size_t)(i0 + u) * ldy] : 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            float y = 0.f;
+            if (i0 + u < Tb) {
+#pragma unroll
+                for (int k = 0; k < PPT; ++k) {
+                    s[k] = make_float2(fmaf(l[k].x, s[k].x, fmaf(-l[k].y, s[k].y, bq[k].x * uin[u])),
+                                       fmaf(l[k].x, s[k].y, fmaf(l[k].y, s[k].x, bq[k].y * uin[u])));
+                    y = fmaf(cq[k].x, s[k].x, fmaf(-cq[k].y, s[k].y, y));
+                }
+                if (!commit) {
+                    float2* rp = ret + (((size_t)bc * Tb + i0 + u) * d + ch) * NP + k0;
+                    if (PPT >= 2) {
+#pragma unroll
+                        for (int k = 0; k < PPT; k += 2)
+                            *reinterpret_cast<float4*>(rp + k) = make_float4(s[k].x, s[k].y, s[k + 1].x, s[k + 1].y);
+                    } else {
+                        rp[0] = s[0];
+                    }
+                }
+            }
+            q[u] = y;
+        }
+#pragma unroll
+        for (int o = LPC / 2; o > 0; o >>= 1)
+#pragma unroll
+            for (int u = 0; u < 8; ++u) q[u] += __shfl_xor_sync(0xffffffffu, q[u], o);
+        if (k0 == 0) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (i0 + u < Tb) out[((size_t)bc * Tb + i0 + u) * d + ch] = from_f32<T>(q[u]);
+        }
+    }
+    if (commit) {
+#pragma unroll
+        for (int k = 0; k < PPT; ++k) state[((size_t)b * d + ch) * NP + k0 + k] = s[k];
+    }
+}
+
 // =========================================================================================
 // Block K/V rows from the fused QKV projection output into the cache (one candidate)
 // or the per-candidate side buffer.
@@ -894,11 +963,32 @@ void launch_iir(evs_handle* h, int li, const Pass& p) {
 #define EVS_IIR(TY, NP)                                                                                       \
     launch_k(h, iir_kernel<TY, NP>, dim3(grid), dim3(256), 0, h->y, 3 * d, (TY*)h->act, d, N, p.C, p.T, p.commit, \
              lam, bb, cc, L.state, L.ret)
-    if (is_bf16(h)) {
-        if (N == 16) EVS_IIR(bf16, 16); else EVS_IIR(bf16, 0);
+#define EVS_IIRC(TY, NP)                                                                                      \
+    launch_k(h, iir_quad_kernel<TY, NP>, dim3((d * (NP < 4 ? 1 : NP / 4) + 255) / 256, p.B * p.C), dim3(256), 0,     \
+             h->y, 3 * d, (TY*)h->act, d, p.C, p.T, p.commit, lam, bb, cc, L.state, L.ret)
+    const int lpc = N < 4 ? 1 : N / 4;
+    if ((d * lpc) % 32 != 0) {   // the quad kernel's early exit must take whole warps
+        if (is_bf16(h)) EVS_IIR(bf16, 0); else EVS_IIR(float, 0);
+    } else if (is_bf16(h)) {
+        switch (N) {
+            case 1: EVS_IIRC(bf16, 1); break;
+            case 2: EVS_IIRC(bf16, 2); break;
+            case 4: EVS_IIRC(bf16, 4); break;
+            case 8: EVS_IIRC(bf16, 8); break;
+            case 16: EVS_IIRC(bf16, 16); break;
+            default: EVS_IIR(bf16, 0); break;
+        }
     } else {
-        if (N == 16) EVS_IIR(float, 16); else EVS_IIR(float, 0);
+        switch (N) {
+            case 1: EVS_IIRC(float, 1); break;
+            case 2: EVS_IIRC(float, 2); break;
+            case 4: EVS_IIRC(float, 4); break;
+            case 8: EVS_IIRC(float, 8); break;
+            case 16: EVS_IIRC(float, 16); break;
+            default: EVS_IIR(float, 0); break;
+        }
     }
+#undef EVS_IIRC
 #undef EVS_IIR
     h->launches++;
     prof_end(h, EVS_K_IIR);
