@@ -224,25 +224,27 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
         for (int j = 0; j < 16; ++j) w[j] = (on && j < L) ? p.taps[(size_t)n * L + j] : 0.f;
     };
-    // IIR item: one (g, channel, pole); pole lambda, input weight B, readout weight C, state
-    auto iir_load = [&](int it, float2& l, float2& bq, float2& cq, float2& sv) {
-        const int N = p.mix_param;
-        l = bq = cq = sv = make_float2(0.f, 0.f);
-        if (it < mgroups * mcw * N) {
-            const int k = it % N, n = n0 + mc_lo + (it / N) % mcw, b = (it / (N * mcw)) / p.mix_C;
-            l = p.lam[(size_t)n * N + k];
-            bq = p.bq[(size_t)n * N + k];
-            cq = p.cq[(size_t)n * N + k];
-            sv = p.state[((size_t)b * p.d + n) * N + k];
+    // IIR item: one (g, channel, quad of four poles); pole lambda, input weight B, readout
+    // weight C and carried state of the quad's poles
+    auto iir_load = [&](int it, float2 (&l)[4], float2 (&bq)[4], float2 (&cq)[4], float2 (&sv)[4]) {
+        const int N = p.mix_param, Q = N / 4;
+        const bool on = it < mgroups * mcw * Q;
+        const int k0 = on ? (it % Q) * 4 : 0, n = n0 + mc_lo + (on ? (it / Q) % mcw : 0);
+        const int b = on ? (it / (Q * mcw)) / p.mix_C : 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            l[k] = on ? p.lam[(size_t)n * N + k0 + k] : make_float2(0.f, 0.f);
+            bq[k] = on ? p.bq[(size_t)n * N + k0 + k] : make_float2(0.f, 0.f);
+            cq[k] = on ? p.cq[(size_t)n * N + k0 + k] : make_float2(0.f, 0.f);
+            sv[k] = on ? p.state[((size_t)b * p.d + n) * N + k0 + k] : make_float2(0.f, 0.f);
         }
     };
     float fw[16];
-    float2 il0, ib0, ic0, is0, il1, ib1, ic1, is1;
+    float2 il[4], ib[4], ic[4], is[4];
     if (p.mix == 1) {
         fir_load(threadIdx.x, fw);
     } else if (p.mix == 2) {
-        iir_load(threadIdx.x, il0, ib0, ic0, is0);
-        iir_load(threadIdx.x + blockDim.x, il1, ib1, ic1, is1);
+        iir_load(threadIdx.x, il, ib, ic, is);
     }
     if (p.ssq_in && warp >= 2) {
         // 1/rms of each token row from the per-tile sums of squares of h, computed by the two
@@ -492,85 +494,53 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
             }
         } else if (p.mix == 2) {
-            // modal IIR: items (group, channel, pole), two per thread per round, their
-            // recurrences interleaved. The serial loop keeps only the state update; the
-            // per-pole readouts and (verify) the states go to shared memory, and after the
-            // loop a thread per (group, position, channel) sums the readout over the poles
-            // and the retained states are copied out with coalesced stores.
-            const int N = p.mix_param;
-            const int items = groups * cw * N;
-            const int nt = blockDim.x, round_items = 2 * nt;
-            // buffers after the partials and vals, 16-byte aligned: [T][round_items] each
-            const size_t used_f = S == 1 ? (size_t)p.M * TC_BM : (size_t)S * p.M * cwm + (size_t)p.M * cw;
-            float* qbuf = park + (used_f + 3) / 4 * 4;
-            float2* sbuf = reinterpret_cast<float2*>(qbuf + (size_t)T * round_items);
-            for (int base = 0; base < items; base += round_items) {
-                const int it0 = base + threadIdx.x, it1 = it0 + nt;
-                if (base > 0) {
-                    iir_load(it0, il0, ib0, ic0, is0);
-                    iir_load(it1, il1, ib1, ic1, is1);
-                    __syncthreads();                  // the previous round's buffers are read
-                }
-                const bool on0 = it0 < items && !bad, on1 = it1 < items && !bad;
-                const int c0 = (it0 / N) % cw, g0 = min(it0 / (N * cw), groups - 1);
-                const int c1 = (it1 / N) % cw, g1 = min(it1 / (N * cw), groups - 1);
-                const float* v0 = vals + (size_t)g0 * T * vld + voff + c0;
-                const float* v1 = vals + (size_t)g1 * T * vld + voff + c1;
-                const float* r0 = rinv_s + g0 * T;
-                const float* r1 = rinv_s + g1 * T;
-                float* q = qbuf + threadIdx.x;
-                float2* sv = sbuf + threadIdx.x;
-                for (int t = 0; t < T; ++t) {
-                    float u0 = on0 ? v0[(size_t)t * vld] : 0.f, u1 = on1 ? v1[(size_t)t * vld] : 0.f;
-                    if (p.ssq_in) {
-                        u0 *= r0[t];
-                        u1 *= r1[t];
-                    }
-                    is0 = make_float2(fmaf(il0.x, is0.x, fmaf(-il0.y, is0.y, ib0.x * u0)),
-                                      fmaf(il0.x, is0.y, fmaf(il0.y, is0.x, ib0.y * u0)));
-                    is1 = make_float2(fmaf(il1.x, is1.x, fmaf(-il1.y, is1.y, ib1.x * u1)),
-                                      fmaf(il1.x, is1.y, fmaf(il1.y, is1.x, ib1.y * u1)));
-                    q[(size_t)t * round_items] = fmaf(ic0.x, is0.x, -ic0.y * is0.y);
-                    q[(size_t)t * round_items + nt] = fmaf(ic1.x, is1.x, -ic1.y * is1.y);
-                    if (!p.mix_commit) {
-                        sv[(size_t)t * round_items] = is0;
-                        sv[(size_t)t * round_items + nt] = is1;
-                    }
-                }
-                if (p.mix_commit) {
-                    const int k0 = it0 % N, k1 = it1 % N;
-                    if (on0) p.state[((size_t)(g0 / p.mix_C) * p.d + n0 + c_lo + c0) * N + k0] = is0;
-                    if (on1) p.state[((size_t)(g1 / p.mix_C) * p.d + n0 + c_lo + c1) * N + k1] = is1;
-                }
-                __syncthreads();
-                if (!bad) {
-                    // readout: the round's (group, channel) pairs (256 / N of them, a power of
-                    // two dividing the 128 threads); thread = pair, positions strided
-                    const int pairs = round_items / N, pl = threadIdx.x % pairs;
-                    const int pr = base / N + pl;
-                    if (pr * N < items) {
-                        const int c = pr % cw, g = pr / cw;
-                        __nv_bfloat16* yo = p.mix_out + (size_t)g * T * p.d + n0 + c_lo + c;
-                        for (int t = threadIdx.x / pairs; t < T; t += nt / pairs) {
-                            const float* qq = qbuf + (size_t)t * round_items + pl * N;
-                            float y = 0.f;
-                            for (int k = 0; k < N; ++k) y += qq[k];
-                            yo[(size_t)t * p.d] = __float2bfloat16_rn(y);
+            // modal IIR: a thread per (group, channel, quad of four poles); the readout of
+            // eight positions at a time is reduced over the channel's N/4 lanes side by side,
+            // and a thread's four retained states of a position are one 32-byte run
+            const int N = p.mix_param, Q = N / 4;
+            const int items = groups * cw * Q;
+            const int span = (items + 31) / 32 * 32;              // whole warps take part
+            for (int it = threadIdx.x; it < span; it += blockDim.x) {
+                if (it != (int)threadIdx.x) iir_load(it, il, ib, ic, is);
+                const bool on = it < items && !bad;
+                const int k0 = (it % Q) * 4, c = (it / Q) % cw, g = min(it / (Q * cw), groups - 1);
+                const int n = n0 + c_lo + c;
+                const float* vr = vals + (size_t)g * T * vld + voff + c;
+                const float* rr = rinv_s + g * T;
+                for (int t0 = 0; t0 < T; t0 += 8) {
+                    float q[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        float y = 0.f;
+                        if (t0 + u < T) {
+                            const float uu = on ? vr[(size_t)(t0 + u) * vld] * (p.ssq_in ? rr[t0 + u] : 1.f) : 0.f;
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                is[k] = make_float2(fmaf(il[k].x, is[k].x, fmaf(-il[k].y, is[k].y, ib[k].x * uu)),
+                                                    fmaf(il[k].x, is[k].y, fmaf(il[k].y, is[k].x, ib[k].y * uu)));
+                                y = fmaf(ic[k].x, is[k].x, fmaf(-ic[k].y, is[k].y, y));
+                            }
+                            if (on && !p.mix_commit) {
+                                float4* rp = reinterpret_cast<float4*>(
+                                    p.ret + (((size_t)g * T + t0 + u) * p.d + n) * N + k0);
+                                rp[0] = make_float4(is[0].x, is[0].y, is[1].x, is[1].y);
+                                rp[1] = make_float4(is[2].x, is[2].y, is[3].x, is[3].y);
+                            }
                         }
+                        q[u] = y;
                     }
-                    if (!p.mix_commit) {
-                        // retained states [g][t][d][N]: this thread's two items, every position;
-                        // a warp's items are contiguous in the buffer and in memory
-                        const size_t tstride = (size_t)p.d * N;
-                        if (on0)
-                            for (int t = 0; t < T; ++t)
-                                p.ret[((size_t)g0 * T * p.d + n0 + c_lo + c0) * N + it0 % N + t * tstride] =
-                                    sbuf[(size_t)t * round_items + threadIdx.x];
-                        if (on1)
-                            for (int t = 0; t < T; ++t)
-                                p.ret[((size_t)g1 * T * p.d + n0 + c_lo + c1) * N + it1 % N + t * tstride] =
-                                    sbuf[(size_t)t * round_items + nt + threadIdx.x];
+                    for (int o = Q >> 1; o > 0; o >>= 1)
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) q[u] += __shfl_xor_sync(0xffffffffu, q[u], o);
+                    if (on && k0 == 0) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            if (t0 + u < T) p.mix_out[((size_t)g * T + t0 + u) * p.d + n] = __float2bfloat16_rn(q[u]);
                     }
+                }
+                if (on && p.mix_commit) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) p.state[((size_t)(g / p.mix_C) * p.d + n) * N + k0 + k] = is[k];
                 }
             }
         }
@@ -846,10 +816,9 @@ bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, flo
             const evs_layer_weights& LW = h->w.layer[fz->mix_layer];
             const int cw = (TC_BM + t.splits - 1) / t.splits;
             size_t need = t.splits > 1 ? (size_t)(t.splits + 1) * M * cw * 4 : (size_t)M * TC_BM * 4;
-            if (L.kind == EVS_LAYER_IIR)   // readout and state buffers of one round (2 x 128 items)
-                need = (need + 15) / 16 * 16 + (size_t)ps->T * 256 * 12;
+
             const bool shape_ok = (t.splits == 1 || t.cluster) && need <= ring && M % ps->T == 0 &&
-                                  (L.kind == EVS_LAYER_FIR || (32 % L.param == 0 && L.param >= 2));
+                                  (L.kind == EVS_LAYER_FIR || (L.param % 4 == 0 && L.param <= 32));
             if (shape_ok) {
                 a.mix = L.kind == EVS_LAYER_FIR ? 1 : 2;
                 a.mix_C = ps->C;
