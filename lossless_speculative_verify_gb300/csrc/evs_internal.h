@@ -37,6 +37,7 @@ struct Geometry {
 // Prefix chunking of the tensor-core attention for one pass shape (attn_fa.cu).
 struct AttnPlan {
     int ok;          // 1 if the tensor-core kernel takes this pass
+    int runs;        // 1: persistent grid over runs of key tiles; 0: one CTA per chunk
     int n_q;         // query rows of the products (128, padded)
     int tiles;       // most 128-key tiles a CTA streams
     int splits;      // chunks of the prefix per sequence and head
@@ -128,7 +129,8 @@ void launch_gemm(evs_handle* h, const void* A, const void* W, float* Y, int M, i
 bool gemm_tc_supported(int M, int N, int K);
 int gemm_tc_init();
 int tc_cta_target();
-// tcgen05 attention (attn_fa.cu)
+// tcgen05 attention (attn_fa.cu): a persistent grid of kAttnGrid CTAs
+constexpr int kAttnGrid = 152;
 AttnPlan attn_plan(int Q, int B, int H, int t_max, int smem_max);
 int attn_init();
 bool launch_attn_tensor(evs_handle* h, int layer, const Pass& p, const AttnPlan& plan);

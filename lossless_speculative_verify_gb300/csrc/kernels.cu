@@ -447,7 +447,7 @@ template <typename T, int EPL>
 __global__ void __launch_bounds__(128, 4) attn_combine_kernel(
     const float* __restrict__ Y, int ldy, const T* __restrict__ kc, const T* __restrict__ vc,
     const T* __restrict__ ks, const T* __restrict__ vs, int H, int dh, int C, int Tb, int Q, int q_max,
-    int t_max, int splits, int chunk, int in_cache, const int32_t* __restrict__ kv_base,
+    int t_max, int splits, int chunk, int B, int fa_grid, int in_cache, const int32_t* __restrict__ kv_base,
     const float* __restrict__ part, T* __restrict__ out, int d) {
     // dependents launch only once the attention partials are complete: an output projection
     // starting earlier would stream its weights against the attention kernel's K / V reads
@@ -467,7 +467,27 @@ __global__ void __launch_bounds__(128, 4) attn_combine_kernel(
     const int qi = c * Tb + i;
     const int n = kv_base[b];  // rows n + j past t_max were never written (overflow flag set);
                                // their reads are clamped to stay in bounds
-    const int used = chunk > 0 ? min((n + chunk - 1) / chunk, splits) : splits;
+    // partial slots of this (sequence, head): chunk > 0, fixed chunks of the prefix (the first
+    // ceil(n / chunk) slots); fa_grid > 0, the persistent tensor-core kernel's runs of key tiles
+    // laid end to end over fa_grid CTAs (one slot per CTA whose run meets this prefix)
+    int used = chunk > 0 ? min((n + chunk - 1) / chunk, splits) : splits;
+    if (fa_grid > 0) {
+        long long total = 0, start = 0;
+        int ntb = 0;
+        for (int bb = 0; bb < B; ++bb) {
+            const int nt = (kv_base[bb] + 127) / 128;
+            if (bb < b) start += (long long)H * nt;
+            if (bb == b) ntb = nt;
+            total += (long long)H * nt;
+        }
+        start += (long long)hh * ntb;
+        used = 0;
+        if (ntb > 0) {
+            const long long W = (total + fa_grid - 1) / fa_grid;
+            used = (int)((start + ntb - 1) / W - start / W + 1);
+        }
+        used = min(used, splits);
+    }
     const float scale = rsqrtf((float)dh);
     const int e0 = lane * EPL;
     const bool act = e0 < dh;
@@ -1018,10 +1038,11 @@ void launch_attention(evs_handle* h, int li, const Pass& p) {
     const int Q = p.C * p.T;
     const Geometry& g = h->g;
     const AttnPlan& plan = p.commit ? h->plan_prefill : h->plan_verify;
-    int splits = g.kv_splits, chunk = g.kv_chunk;
+    int splits = g.kv_splits, chunk = g.kv_chunk, fa_grid = 0;
     if (plan.ok && launch_attn_tensor(h, li, p, plan)) {
         splits = plan.splits;
-        chunk = 0;   // equal shares of the prefix over every split
+        chunk = 0;                               // every slot written (empty ones m = -inf)
+        fa_grid = plan.runs ? kAttnGrid : 0;     // or runs of key tiles over the persistent grid
     } else {
     dim3 grid(g.kv_splits, p.B * H, (Q + AQ - 1) / AQ);
     if (is_bf16(h))
@@ -1039,7 +1060,7 @@ void launch_attention(evs_handle* h, int li, const Pass& p) {
 #define EVS_CMB(TY, EPL)                                                                                \
     launch_k(h, attn_combine_kernel<TY, EPL>, dim3(grid2), dim3(128), 0, h->y, 3 * d, (const TY*)L.kc,       \
              (const TY*)L.vc, (const TY*)L.ks, (const TY*)L.vs, H, dh, p.C, p.T, Q, g.q_max, h->cfg.t_max, \
-             splits, chunk, p.kv_in_cache, h->kv_base, h->attn_part, (TY*)h->act, d)
+             splits, chunk, p.B, fa_grid, p.kv_in_cache, h->kv_base, h->attn_part, (TY*)h->act, d)
     if (is_bf16(h)) {
         if (dh > 64) EVS_CMB(bf16, 4); else if (dh > 32) EVS_CMB(bf16, 2); else EVS_CMB(bf16, 1);
     } else {
