@@ -188,6 +188,7 @@ class Pair:
         own = oracle.accept_block(bp["logits"], sub(rnd["tokens"]), sub(rnd["q"]), sub(rnd["u"]),
                                   wl.mode, wl.temperature, TAU[wl.dtype])
         k, corr, cand, tie = self.ver.verify(toks, q, u)
+        self.round_launches = self.ver.launches          # kernels of the verify call
         torch.cuda.synchronize()
         if check_block:
             self.check_block(bp, tol, sq)
@@ -204,6 +205,7 @@ class Pair:
                 (sq[i], gk, gc, gcand, kern[3:6])
         oracle.commit(states, bp, gk, gcand)
         self.ver.slice(k, cand)
+        self.round_launches += self.ver.launches         # plus the slice
         return RoundOut(own, kern, gk, gc, gcand, bp)
 
     def check_block(self, res, tol, sq=None):
