@@ -128,7 +128,7 @@ typedef struct {
 enum {
     EVS_BUF_LOGITS = 0,     /* [B*C*(gamma+1)][vocab] fp32, last verify                 */
     EVS_BUF_FIR_STAGE = 1,  /* layer: [B][C][L-1+gamma+1][d] fp32 = [tail || inputs v]    */
-    EVS_BUF_IIR_RET = 2,    /* layer: [B][C][gamma+1][d][N][2] fp32, s_0..s_gamma         */
+    EVS_BUF_IIR_U = 2,      /* layer: [B][C][gamma+1][d] fp32 scan inputs u_0..u_gamma    */
     EVS_BUF_K_CACHE = 3,    /* layer: [B][H][t_max][dh] dtype                             */
     EVS_BUF_V_CACHE = 4,    /* layer: [B][H][t_max][dh] dtype                             */
     EVS_BUF_K_SIDE = 5,     /* layer, n_cand > 1: [B][C][H][gamma+1][dh] dtype block keys  */

@@ -18,7 +18,7 @@ LAYER_FIR, LAYER_IIR, LAYER_ATTN = 0, 1, 2
 DTYPE_F32, DTYPE_BF16 = 0, 1
 MODE_GREEDY, MODE_SAMPLING = 0, 1
 FLAG_KV_OVERFLOW, FLAG_BAD_K, FLAG_EMPTY_RESIDUAL, FLAG_BAD_TOKEN, FLAG_TIMEOUT = 1, 2, 4, 8, 16
-(BUF_LOGITS, BUF_FIR_STAGE, BUF_IIR_RET, BUF_K_CACHE, BUF_V_CACHE, BUF_K_SIDE, BUF_V_SIDE,
+(BUF_LOGITS, BUF_FIR_STAGE, BUF_IIR_U, BUF_K_CACHE, BUF_V_CACHE, BUF_K_SIDE, BUF_V_SIDE,
  BUF_KV_LEN, BUF_FIR_TAIL, BUF_IIR_STATE, BUF_CAND_K, BUF_CAND_CORR) = range(12)
 
 EXPORTED = (

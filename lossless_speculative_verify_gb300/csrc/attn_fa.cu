@@ -44,7 +44,6 @@ struct FaArgs {
     const float* y;        // projection output, q in columns [head*dh, head*dh + dh)
     int ldy, B, H, Q;      // sequences, heads, queries per sequence (<= 128)
     int splits, q_stride, stages;   // splits: partial slots per (sequence, head)
-    int runs;              // 1: persistent grid over runs of tiles; 0: grid (splits, B*H) of chunks
     float scale;
     const int32_t* kv_base;
     float* part;           // [B][H][splits][q_stride][dh + 2]
@@ -550,7 +549,7 @@ bool launch_attn_tensor(evs_handle* h, int li, const Pass& p, const AttnPlan& pl
     CUtensorMap tk, tv;
     if (!make_kv_map(&tk, L.kc, h->cfg.t_max, p.B * H) || !make_kv_map(&tv, L.vc, h->cfg.t_max, p.B * H))
         return false;
-    FaArgs a{h->y, 3 * h->cfg.d, p.B, H, p.C * p.T, plan.splits, h->g.q_max, plan.stages, plan.runs,
+    FaArgs a{h->y, 3 * h->cfg.d, p.B, H, p.C * p.T, plan.splits, h->g.q_max, plan.stages,
              1.0f / sqrtf((float)FA_DH), h->kv_base, h->attn_part, h->flags};
     if (plan.runs)
         return launch_k(h, attn_fa_kernel<true>, dim3(FA_GRID), dim3(FA_THREADS), (size_t)plan.smem, tk, tv, a) ==

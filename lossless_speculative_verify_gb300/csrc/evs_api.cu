@@ -153,7 +153,7 @@ size_t carve(const evs_config& c, char* base, evs_handle* h) {
         evs::LayerDesc L{};
         L.kind = c.layer_kind[i];
         L.param = c.layer_param[i];
-        size_t tail_b = 0, stage_b = 0, state_b = 0, ret_b = 0, cache_b = 0, side_b = 0;
+        size_t tail_b = 0, stage_b = 0, state_b = 0, uin_b = 0, cache_b = 0, side_b = 0;
         if (L.kind == EVS_LAYER_FIR) {
             tail_b = B * (L.param - 1) * d * 4;
             stage_b = B * C * (L.param - 1 + T) * d * 4;
@@ -161,9 +161,13 @@ size_t carve(const evs_config& c, char* base, evs_handle* h) {
             L.stage = (float*)take(stage_b);
         } else if (L.kind == EVS_LAYER_IIR) {
             state_b = B * d * L.param * 8;
-            ret_b = B * C * T * d * L.param * 8;
+            uin_b = B * C * T * d * 4;
             L.state = (float2*)take(state_b);
-            L.ret = (float2*)take(ret_b);
+            L.uin = (float*)take(uin_b);
+            if (h) {
+                L.lam = (const float2*)h->w.layer[i].iir_lambda;
+                L.bq = (const float2*)h->w.layer[i].iir_b;
+            }
         } else {
             cache_b = B * (size_t)L.param * (size_t)c.t_max * dh * es;
             L.kc = take(cache_b);
@@ -179,7 +183,7 @@ size_t carve(const evs_config& c, char* base, evs_handle* h) {
             h->tail_bytes[i] = tail_b;
             h->stage_bytes[i] = stage_b;
             h->state_bytes[i] = state_b;
-            h->ret_bytes[i] = ret_b;
+            h->uin_bytes[i] = uin_b;
             h->cache_bytes[i] = cache_b;
             h->side_bytes[i] = side_b;
         }
@@ -261,6 +265,13 @@ evs_status zero_state(evs_handle* h) {
     return EVS_OK;
 }
 
+// Where a layer's in-projection leaves the mixer input: a verify pass keeps an IIR layer's
+// scan inputs u_0..u_gamma in the layer's own buffer, from which slicing recomputes s_k;
+// everything else goes through the shared projection output.
+float* mixer_input(evs_handle* h, int li, const evs::Pass& p) {
+    return h->cfg.layer_kind[li] == EVS_LAYER_IIR && !p.commit ? h->layer[li].uin : h->y;
+}
+
 // One block pass through every layer (Lemma 2: a single forward from the pre-round state).
 void run_layers(evs_handle* h, const int32_t* tokens, int tok_stride, const int32_t* anchor,
                 const evs::Pass& p, bool with_head) {
@@ -278,18 +289,21 @@ void run_layers(evs_handle* h, const int32_t* tokens, int tok_stride, const int3
             evs::GemmFuse mixin = in;
             switch (c.layer_kind[li]) {
                 case EVS_LAYER_FIR:
-                case EVS_LAYER_IIR:
+                case EVS_LAYER_IIR: {
                     // the mixer runs in the in-projection's epilogue when the shape allows
                     mixin.mix_layer = h->fuse_mixer ? li : -1;
-                    evs::launch_gemm(h, h->hb, W.w_in, h->y, p.M, d, d, 3 * d, 0, &mixin, &fused);
+                    float* v = mixer_input(h, li, p);
+                    const int ldv = v == h->y ? 3 * d : d;
+                    evs::launch_gemm(h, h->hb, W.w_in, v, p.M, d, d, ldv, 0, &mixin, &fused);
                     if (!(fused & 1)) {
                         if (c.layer_kind[li] == EVS_LAYER_FIR)
                             evs::launch_fir(h, li, p);
                         else
-                            evs::launch_iir(h, li, p);
+                            evs::launch_iir(h, li, p, v, ldv);
                     }
                     evs::launch_gemm(h, h->act, W.w_out, h->h, p.M, d, d, d, 1, &out);
                     break;
+                }
                 default:
                     mixin.kv_layer = li;   // K/V rows written straight from the QKV epilogue
                     evs::launch_gemm(h, h->hb, W.w_qkv, h->y, p.M, 3 * d, d, 3 * d, 0, &mixin, &fused);
@@ -310,11 +324,14 @@ void run_layers(evs_handle* h, const int32_t* tokens, int tok_stride, const int3
                 evs::launch_fir(h, li, p);
                 evs::launch_gemm(h, h->act, W.w_out, h->h, p.M, d, d, d, 1);
                 break;
-            case EVS_LAYER_IIR:
-                evs::launch_gemm(h, h->act, W.w_in, h->y, p.M, d, d, 3 * d, 0);
-                evs::launch_iir(h, li, p);
+            case EVS_LAYER_IIR: {
+                float* v = mixer_input(h, li, p);
+                const int ldv = v == h->y ? 3 * d : d;
+                evs::launch_gemm(h, h->act, W.w_in, v, p.M, d, d, ldv, 0);
+                evs::launch_iir(h, li, p, v, ldv);
                 evs::launch_gemm(h, h->act, W.w_out, h->h, p.M, d, d, d, 1);
                 break;
+            }
             default:
                 evs::launch_gemm(h, h->act, W.w_qkv, h->y, p.M, 3 * d, d, 3 * d, 0);
                 evs::launch_kv_write(h, li, p);
@@ -596,7 +613,7 @@ evs_status evs_debug_buffer(evs_handle* h, int32_t which, int32_t layer, evs_buf
         case EVS_BUF_CAND_CORR: p = h->cand_corr; n = (size_t)c.batch * c.n_cand * 4; break;
         case EVS_BUF_FIR_STAGE: p = L->stage; n = h->stage_bytes[layer]; break;
         case EVS_BUF_FIR_TAIL: p = L->tail; n = h->tail_bytes[layer]; break;
-        case EVS_BUF_IIR_RET: p = L->ret; n = h->ret_bytes[layer]; break;
+        case EVS_BUF_IIR_U: p = L->uin; n = h->uin_bytes[layer]; break;
         case EVS_BUF_IIR_STATE: p = L->state; n = h->state_bytes[layer]; break;
         case EVS_BUF_K_CACHE: p = L->kc; n = h->cache_bytes[layer]; break;
         case EVS_BUF_V_CACHE: p = L->vc; n = h->cache_bytes[layer]; break;

@@ -17,7 +17,9 @@ struct LayerDesc {
     float* tail;                   // FIR [B][L-1][d]
     float* stage;                  // FIR [B][C][L-1+T][d]
     float2* state;                 // IIR [B][d][N]
-    float2* ret;                   // IIR [B][C][T][d][N]
+    float* uin;                    // IIR [B][C][T][d]: the verify pass's scan inputs u_t
+    const float2* lam;             // IIR [d][N] poles and input weights (the slice kernel
+    const float2* bq;              // recomputes s_k from the state and u_0..u_k)
     void* kc;                      // attn [B][H][t_max][dh]
     void* vc;
     void* ks;                      // attn, C > 1: [B][C][H][T][dh]
@@ -100,7 +102,7 @@ struct evs_handle {
     evs::LayerDesc layer[EVS_MAX_LAYERS];
     evs::LayerDesc* layer_dev;   // device copy
     // sizes of per-layer buffers (bytes), for evs_debug_buffer
-    size_t stage_bytes[EVS_MAX_LAYERS], ret_bytes[EVS_MAX_LAYERS], cache_bytes[EVS_MAX_LAYERS],
+    size_t stage_bytes[EVS_MAX_LAYERS], uin_bytes[EVS_MAX_LAYERS], cache_bytes[EVS_MAX_LAYERS],
         side_bytes[EVS_MAX_LAYERS], tail_bytes[EVS_MAX_LAYERS], state_bytes[EVS_MAX_LAYERS];
     // host bookkeeping
     long long kv_hi;      // host upper bound of max_b kv_len
@@ -139,7 +141,7 @@ bool make_kv_map(CUtensorMap* m, const void* base, int t_max, int bh);
 bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, float* Y, int M, int N,
                     int K, int ldy, int accumulate, const GemmFuse* fz = nullptr, int* fused = nullptr);
 void launch_fir(evs_handle* h, int layer, const Pass& p);
-void launch_iir(evs_handle* h, int layer, const Pass& p);
+void launch_iir(evs_handle* h, int layer, const Pass& p, const float* u, int ldu);
 void launch_kv_write(evs_handle* h, int layer, const Pass& p);
 void launch_attention(evs_handle* h, int layer, const Pass& p);
 void launch_accept(evs_handle* h, const int32_t* tokens, const float* q, const float* u,

@@ -80,7 +80,7 @@ struct TcArgs {
     const float2* bq;
     const float2* cq;
     float2* state;
-    float2* ret;
+    float* uin;       // IIR, verify: the scan inputs u_t [M][d] kept for slicing
     // fused K/V write of an attention layer's QKV projection: columns [d, 3d) go to the
     // cache (one candidate) or the per-candidate side buffer instead of Y
     int kv, kv_H, kv_dh, kv_in_cache, kv_tmax, kv_C, kv_T;
@@ -495,8 +495,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
         } else if (p.mix == 2) {
             // modal IIR: a thread per (group, channel, quad of four poles); the readout of
-            // eight positions at a time is reduced over the channel's N/4 lanes side by side,
-            // and a thread's four retained states of a position are one 32-byte run
+            // eight positions at a time is reduced over the channel's N/4 lanes side by side.
+            // A verify pass keeps the inputs u_t (slicing recomputes s_k from them).
             const int N = p.mix_param, Q = N / 4;
             const int items = groups * cw * Q;
             const int span = (items + 31) / 32 * 32;              // whole warps take part
@@ -520,12 +520,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                                     fmaf(il[k].x, is[k].y, fmaf(il[k].y, is[k].x, ib[k].y * uu)));
                                 y = fmaf(ic[k].x, is[k].x, fmaf(-ic[k].y, is[k].y, y));
                             }
-                            if (on && !p.mix_commit) {
-                                float4* rp = reinterpret_cast<float4*>(
-                                    p.ret + (((size_t)g * T + t0 + u) * p.d + n) * N + k0);
-                                rp[0] = make_float4(is[0].x, is[0].y, is[1].x, is[1].y);
-                                rp[1] = make_float4(is[2].x, is[2].y, is[3].x, is[3].y);
-                            }
+                            if (on && !p.mix_commit && k0 == 0) p.uin[((size_t)g * T + t0 + u) * p.d + n] = uu;
                         }
                         q[u] = y;
                     }
@@ -833,7 +828,7 @@ bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, flo
                 a.bq = (const float2*)LW.iir_b;
                 a.cq = (const float2*)LW.iir_c;
                 a.state = L.state;
-                a.ret = L.ret;
+                a.uin = L.uin;
                 did |= 1;
             }
         }

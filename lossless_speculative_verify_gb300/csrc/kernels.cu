@@ -171,14 +171,14 @@ __global__ void fir_kernel(const float* __restrict__ Y, int ldy, T* __restrict__
 // =========================================================================================
 // Modal IIR scan s_t = lam * s_{t-1} + b * u_t, y_t = Re sum_n c_n s_{t,n}.
 // N consecutive lanes hold the N poles of one channel; y by a shuffle reduction.
-// Every s_t goes to the retained-state buffer (verify), or the last one to the state
-// (prefill).
+// A prefill pass (commit) leaves the last s_t in the state. A verify pass writes no state:
+// its inputs u_t stay where the in-projection put them, and slicing recomputes s_k.
 // =========================================================================================
 template <typename T, int NP>   // NP: poles per channel when fixed at compile time, else 0
 __global__ void __launch_bounds__(256) iir_kernel(const float* __restrict__ Y, int ldy, T* __restrict__ out, int d,
                                                   int Nrt, int C, int Tb, int commit, const float2* __restrict__ lam,
                                                   const float2* __restrict__ bb, const float2* __restrict__ cc,
-                                                  float2* __restrict__ state, float2* __restrict__ ret) {
+                                                  float2* __restrict__ state) {
     pdl_trigger();
     pdl_wait();
     const int N = NP > 0 ? NP : Nrt;
@@ -189,9 +189,7 @@ __global__ void __launch_bounds__(256) iir_kernel(const float* __restrict__ Y, i
     const float2 l = lam[g], bq = bb[g], cq = cc[g];
     float2 s = state[(size_t)b * d * N + g];
     const float* yin = Y + (size_t)bc * Tb * ldy + ch;
-    float2* rp = ret + (size_t)bc * Tb * d * N + g;
     T* op = out + (size_t)bc * Tb * d + ch;
-    const size_t rstride = (size_t)d * N;
     for (int i0 = 0; i0 < Tb; i0 += 8) {
         // eight positions: inputs requested together, the recurrence, then the eight
         // readouts reduced over the pole lanes side by side
@@ -203,7 +201,6 @@ __global__ void __launch_bounds__(256) iir_kernel(const float* __restrict__ Y, i
             if (i0 + k < Tb) {
                 const float u = uin[k];
                 s = make_float2(fmaf(l.x, s.x, fmaf(-l.y, s.y, bq.x * u)), fmaf(l.x, s.y, fmaf(l.y, s.x, bq.y * u)));
-                if (!commit) rp[(size_t)(i0 + k) * rstride] = s;
             }
             q[k] = fmaf(cq.x, s.x, -cq.y * s.y);
         }
@@ -224,14 +221,12 @@ __global__ void __launch_bounds__(256) iir_kernel(const float* __restrict__ Y, i
 }
 
 // The same scan with four poles per thread (N/4 lanes per channel): the readout needs only
-// log2(N/4) shuffle levels, and a thread's four retained states of a position are one
-// 32-byte run, so a warp writes eight channels' states as one contiguous kilobyte.
+// log2(N/4) shuffle levels.
 template <typename T, int NP>
 __global__ void __launch_bounds__(256) iir_quad_kernel(const float* __restrict__ Y, int ldy, T* __restrict__ out,
                                                        int d, int C, int Tb, int commit,
                                                        const float2* __restrict__ lam, const float2* __restrict__ bb,
-                                                       const float2* __restrict__ cc, float2* __restrict__ state,
-                                                       float2* __restrict__ ret) {
+                                                       const float2* __restrict__ cc, float2* __restrict__ state) {
     constexpr int PPT = NP < 4 ? NP : 4;     // poles per thread
     constexpr int LPC = NP / PPT;            // lanes per channel
     pdl_trigger();
@@ -262,16 +257,6 @@ __global__ void __launch_bounds__(256) iir_quad_kernel(const float* __restrict__
                     s[k] = make_float2(fmaf(l[k].x, s[k].x, fmaf(-l[k].y, s[k].y, bq[k].x * uin[u])),
                                        fmaf(l[k].x, s[k].y, fmaf(l[k].y, s[k].x, bq[k].y * uin[u])));
                     y = fmaf(cq[k].x, s[k].x, fmaf(-cq[k].y, s[k].y, y));
-                }
-                if (!commit) {
-                    float2* rp = ret + (((size_t)bc * Tb + i0 + u) * d + ch) * NP + k0;
-                    if (PPT >= 2) {
-#pragma unroll
-                        for (int k = 0; k < PPT; k += 2)
-                            *reinterpret_cast<float4*>(rp + k) = make_float4(s[k].x, s[k].y, s[k + 1].x, s[k + 1].y);
-                    } else {
-                        rp[0] = s[0];
-                    }
                 }
             }
             q[u] = y;
@@ -839,8 +824,10 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(
 // =========================================================================================
 // State slicing at k (Figure 1(d)): FIR tail <- stage rows k+1 .. k+L-1, IIR state <- s_k,
 // and for several candidates the chosen candidate's k+1 block K/V rows into the cache;
-// then kv_len = kv_base + k + 1. Grid (B, layers, blocks per layer): every layer's copy runs
-// in parallel, 16 bytes per thread where the rows allow it.
+// then kv_len = kv_base + k + 1. Grid (B, layers, blocks per layer): every layer runs in
+// parallel, copies 16 bytes per thread where the rows allow it. s_k is not stored by the
+// verify pass: it is k+1 steps of the diagonal recurrence from the pre-round state over the
+// kept inputs, (k+1) d floats read instead of gamma+1 states of d N complex values written.
 // =========================================================================================
 template <typename T>
 __global__ void slice_kernel(const LayerDesc* __restrict__ layers, int n_layers, int d, int dh,
@@ -870,10 +857,43 @@ __global__ void slice_kernel(const LayerDesc* __restrict__ layers, int n_layers,
         float4* dst = reinterpret_cast<float4*>(L.tail + (size_t)b * Lm1 * d);
         for (int e = start; e < Lm1 * d / 4; e += stride) dst[e] = src[e];   // d % 64 == 0
     } else if (L.kind == EVS_LAYER_IIR) {
-        const int n = d * L.param;                 // float2 elements, n even
-        const float4* src = reinterpret_cast<const float4*>(L.ret + ((size_t)bc * Tb + k) * n);
-        float4* dst = reinterpret_cast<float4*>(L.state + (size_t)b * n);
-        for (int e = start; e < n / 2; e += stride) dst[e] = src[e];
+        // s_k from the pre-round state and the kept inputs u_0..u_k, by the scan's own
+        // operations in the scan's order: the value the scan reached at position k. An item
+        // is up to four poles of one channel, so each input load serves four recurrences.
+        const int N = L.param, ppt = N < 4 ? N : 4, qpc = N / ppt;
+        const float* u = L.uin + (size_t)bc * Tb * d;
+        float2* st = L.state + (size_t)b * d * N;
+        for (int it = start; it < d * qpc; it += stride) {
+            const int ch = it / qpc;
+            const size_t base = (size_t)ch * N + (size_t)(it % qpc) * ppt;
+            float2 l[4], bq[4], s[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (q < ppt) {
+                    l[q] = L.lam[base + q];
+                    bq[q] = L.bq[base + q];
+                    s[q] = st[base + q];
+                }
+            }
+            for (int j0 = 0; j0 <= k; j0 += 8) {
+                float uv[8];   // eight inputs requested before the recurrence uses any
+#pragma unroll
+                for (int j = 0; j < 8; ++j) uv[j] = j0 + j <= k ? u[(size_t)(j0 + j) * d + ch] : 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (j0 + j <= k) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (q < ppt)
+                                s[q] = make_float2(fmaf(l[q].x, s[q].x, fmaf(-l[q].y, s[q].y, bq[q].x * uv[j])),
+                                                   fmaf(l[q].x, s[q].y, fmaf(l[q].y, s[q].x, bq[q].y * uv[j])));
+                    }
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (q < ppt) st[base + q] = s[q];
+        }
     } else if (C > 1 && !overflow) {
         const int H = L.param;
         const int per = (k + 1) * dh;
@@ -971,7 +991,7 @@ void launch_fir(evs_handle* h, int li, const Pass& p) {
     prof_end(h, EVS_K_FIR);
 }
 
-void launch_iir(evs_handle* h, int li, const Pass& p) {
+void launch_iir(evs_handle* h, int li, const Pass& p, const float* u, int ldu) {
     prof_begin(h, EVS_K_IIR);
     const int d = h->cfg.d;
     const LayerDesc& L = h->layer[li];
@@ -981,11 +1001,11 @@ void launch_iir(evs_handle* h, int li, const Pass& p) {
     const float2* bb = (const float2*)h->w.layer[li].iir_b;
     const float2* cc = (const float2*)h->w.layer[li].iir_c;
 #define EVS_IIR(TY, NP)                                                                                       \
-    launch_k(h, iir_kernel<TY, NP>, dim3(grid), dim3(256), 0, h->y, 3 * d, (TY*)h->act, d, N, p.C, p.T, p.commit, \
-             lam, bb, cc, L.state, L.ret)
+    launch_k(h, iir_kernel<TY, NP>, dim3(grid), dim3(256), 0, u, ldu, (TY*)h->act, d, N, p.C, p.T, p.commit, lam, \
+             bb, cc, L.state)
 #define EVS_IIRC(TY, NP)                                                                                      \
     launch_k(h, iir_quad_kernel<TY, NP>, dim3((d * (NP < 4 ? 1 : NP / 4) + 255) / 256, p.B * p.C), dim3(256), 0,     \
-             h->y, 3 * d, (TY*)h->act, d, p.C, p.T, p.commit, lam, bb, cc, L.state, L.ret)
+             u, ldu, (TY*)h->act, d, p.C, p.T, p.commit, lam, bb, cc, L.state)
     const int lpc = N < 4 ? 1 : N / 4;
     if ((d * lpc) % 32 != 0) {   // the quad kernel's early exit must take whole warps
         if (is_bf16(h)) EVS_IIR(bf16, 0); else EVS_IIR(float, 0);
@@ -1097,7 +1117,16 @@ void launch_accept(evs_handle* h, const int32_t* tokens, const float* q, const f
 void launch_slice(evs_handle* h, const int32_t* k, const int32_t* cand) {
     prof_begin(h, EVS_K_SLICE);
     const evs_config& c = h->cfg;
-    dim3 grid(c.batch, c.n_layers, 8);
+    // blocks per layer: enough for one item per thread on the largest layer (an IIR layer's
+    // channels x pole quads, a FIR tail in float4, a candidate's K/V rows), 8 to 64
+    long long items = 0;
+    for (int i = 0; i < c.n_layers; ++i) {
+        const int kind = c.layer_kind[i], prm = c.layer_param[i];
+        if (kind == EVS_LAYER_IIR) items = std::max(items, (long long)c.d * std::max(prm / 4, 1));
+        else if (kind == EVS_LAYER_FIR) items = std::max(items, (long long)(prm - 1) * c.d / 4);
+        else if (c.n_cand > 1) items = std::max(items, (long long)c.d * (c.gamma + 1));
+    }
+    dim3 grid(c.batch, c.n_layers, (unsigned)std::min(64LL, std::max(8LL, (items + 255) / 256)));
     if (is_bf16(h))
         launch_k(h, slice_kernel<bf16>, dim3(grid), dim3(256), 0, h->layer_dev, c.n_layers, c.d, c.head_dim, c.n_cand,
             c.gamma + 1, c.gamma, c.t_max, k, cand, h->kv_base, h->kv_len, h->flags);

@@ -193,7 +193,7 @@ class Target:
                 y, S["s"] = iir_step(S["s"], u, L["lam"], L["b"], L["c"])
                 h = h + y @ L["w_out"]
                 if trace is not None:
-                    trace.append({"kind": "iir", "s": S["s"].copy()})
+                    trace.append({"kind": "iir", "s": S["s"].copy(), "u": u})
             else:
                 H, dh = L["H"], L["dh"]
                 q = (xh @ L["wq"]).reshape(H, dh)
@@ -248,7 +248,7 @@ class Target:
                 s_all = s_forced + s_free                           # [T, d, N]
                 y = np.real(np.sum(c[None] * s_all, axis=2))
                 h = h + y @ L["w_out"]
-                layer_vals.append({"kind": "iir", "s": s_all})
+                layer_vals.append({"kind": "iir", "s": s_all, "u": u})
             else:
                 H, dh = L["H"], L["dh"]
                 q = (xh @ L["wq"]).reshape(T, H, dh)

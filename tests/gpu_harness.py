@@ -209,7 +209,9 @@ class Pair:
         return RoundOut(own, kern, gk, gc, gcand, bp)
 
     def check_block(self, res, tol, sq=None):
-        """Block forward outputs: logits, retained IIR states, FIR inputs, block K/V."""
+        """Block forward outputs: logits, IIR scan inputs, FIR inputs, block K/V. (Each IIR
+        state s_t enters the logits through the readout; the sliced s_k is compared after
+        the slice.)"""
         res = _Res(res)
         wl = self.wl
         B, C, T, V, d = wl.batch, wl.n_cand, wl.block, wl.vocab, wl.d
@@ -219,12 +221,11 @@ class Pair:
         assert e <= tol, f"logits rel err {e:.3e}"
         for li, spec in enumerate(wl.layers):
             if spec.kind == "iir":
-                N = spec.param
-                ret = self.ver.buffer(2, li, torch.float32, (B, C, T, d, N, 2)).cpu().numpy()[sq]
-                ref = np.array([[[res.traces[b][c][i][li]["s"] for i in range(T)] for c in range(C)]
+                uin = self.ver.buffer(2, li, torch.float32, (B, C, T, d)).cpu().numpy()[sq]
+                ref = np.array([[[res.traces[b][c][i][li]["u"] for i in range(T)] for c in range(C)]
                                 for b in range(len(sq))])
-                e = rel_l2(ret, np.stack([ref.real, ref.imag], axis=-1))
-                assert e <= tol, f"layer {li} retained IIR states rel err {e:.3e}"
+                e = rel_l2(uin, ref)
+                assert e <= tol, f"layer {li} IIR scan inputs rel err {e:.3e}"
             elif spec.kind == "fir":
                 Lm1 = spec.param - 1
                 stage = self.ver.buffer(1, li, torch.float32, (B, C, Lm1 + T, d)).cpu().numpy()[sq]

@@ -1,6 +1,6 @@
 """Parity at the full workload sizes, in the launch configuration the benchmark times
 (same handle configuration, kernels and grids), on sampled outputs the fp64 oracle can
-afford: one round from a synthetic pre-round state, every logit and retained state of the
+afford: one round from a synthetic pre-round state, every logit and IIR scan input of the
 sampled sequences, the decisions (in the kernel's precision), and the sliced state
 (kv_len, FIR tails, IIR states, the cache rows the round wrote)."""
 import numpy as np

@@ -1,6 +1,6 @@
 """GPU parity: the CUDA path through the C-ABI against the fp64 oracle, element by
 element on the same seeded inputs. Tolerances: relative L2 error per tensor <= 1e-5 (fp32)
-or 2e-2 (bf16) on logits, retained IIR states, FIR inputs, K/V and sliced states; accepted
+or 2e-2 (bf16) on logits, IIR scan inputs, FIR inputs, K/V and sliced states; accepted
 lengths, corrections, candidates, KV lengths and slice indices exact, except on rounds the
 oracle flags as near-ties (counted). Discrete decisions are compared in the kernel's
 precision: the oracle's acceptance on the library's fp32 logits; the oracle state is then sliced

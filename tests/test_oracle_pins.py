@@ -150,6 +150,7 @@ def test_block_forward_equals_sequential_decode():
                 np.testing.assert_allclose(a["v"], bv["v"][i], atol=1e-11)
             elif a["kind"] == "iir":
                 np.testing.assert_allclose(a["s"], bv["s"][i], atol=1e-10)
+                np.testing.assert_allclose(a["u"], bv["u"][i], atol=1e-11)
             else:
                 np.testing.assert_allclose(a["k"], bv["k"][i], atol=1e-11)
                 np.testing.assert_allclose(a["v"], bv["v"][i], atol=1e-11)
