@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-also", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--no-decode", action="store_true", help="skip the native-decode control leg")
     ap.add_argument("--prefix", type=int, default=None,
                     help="cached tokens per sequence instead of the workload's (small profiling "
                          "cases; the workload name then carries the override)")
@@ -212,7 +213,8 @@ def run_evs(args, wl, rank, world, light=False):
     P, T = wl.prefix_len, wl.block
     n_prof = min(K, 8)
     rounds = W + 2 * K + 2 * n_prof + 2
-    t_max = (P + rounds * T + 255) // 256 * 256
+    dec_steps = W + K + 2                           # native decode steps of the control leg
+    t_max = (P + rounds * T + dec_steps + 255) // 256 * 256
     weights = gen_weights(wl)
     layers = [(s.kind, s.param) for s in wl.layers]
     dw = DeviceWeights(layers, weights, wl.dtype, dev)
@@ -298,8 +300,9 @@ def run_evs(args, wl, rank, world, light=False):
     ms = sum(a.elapsed_time(b) for a, b in evs)
     tokens = int(tok_acc.sum().item())
     clk = clocks.stop() if clocks is not None else None
+    dec_ms = None if args.no_decode else decode_control(args, ver, s, flush, wl, K, W)
     if light:
-        return dict(ms=ms, tokens=tokens, clocks=clk, flags=ver.flags(), graph=graph is not None)
+        return dict(ms=ms, tokens=tokens, clocks=clk, flags=ver.flags(), graph=graph is not None, dec_ms=dec_ms)
     # end-to-end through the public API: pinned host inputs in, accepted length and
     # correction out, every step
     e2e_ms = 0.0
@@ -356,7 +359,54 @@ def run_evs(args, wl, rank, world, light=False):
     ms, e2e_ms, tokens, e2e_tokens = aggregate(ms, e2e_ms, tokens, e2e_tokens, dev)
     return dict(ms=ms, tokens=tokens, e2e_ms=e2e_ms, e2e_tokens=e2e_tokens, h2d=h2d, d2h=d2h,
                 prof=prof, n_prof=n_prof, prof_mode=prof_mode, launches_round=launches_round, clocks=clk,
-                flags=flags, graph=graph is not None)
+                flags=flags, graph=graph is not None, dec_ms=dec_ms)
+
+
+def decode_control(args, ver, s, flush, wl, K, W):
+    """Native decoding on the same handle and state: one token per sequence per step (the
+    target's own loop), timed like the rounds (graph replay, L2 flushed before each step).
+    Returns ms per step."""
+    import torch
+    B = wl.batch
+    dev = ver.next.device
+    g = torch.Generator(device=dev)
+    g.manual_seed(5000 + wl.seed_base)
+    u = torch.rand(B, generator=g, device=dev) if wl.mode == "sampling" else None
+    with torch.cuda.stream(s):
+        ver.next.fill_(65)
+        ver.decode(ver.next, u)                        # eager step: next token in place
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            ver.decode(ver.next, u)
+    step = graph.replay if graph is not None else (lambda: ver.decode(ver.next, u))
+    with torch.cuda.stream(s):
+        for _ in range(W):
+            step()
+    s.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with torch.cuda.stream(s):
+        for i in range(K):
+            flush.zero_()
+            evs[i][0].record(s)
+            step()
+            evs[i][1].record(s)
+    s.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / K
+
+
+def control_line(wl, round_ms, dec_ms):
+    """The identity-drafter control against native throughput: a drafter that always agrees
+    gets every draft accepted, gamma+1 tokens per sequence per round. The round's kernels do
+    the same work whatever the tokens (only the slice copies depend on k), so the measured
+    round time stands for it."""
+    if dec_ms is None:
+        return None
+    B, T = wl.batch, wl.gamma + 1
+    return {"native_us_per_step": round(dec_ms * 1e3, 2), "native_tokens_per_s": B / (dec_ms / 1e3),
+            "identity_drafter_tokens_per_s": B * T / (round_ms / 1e3),
+            "identity_drafter_vs_native": T * dec_ms / round_ms}
 
 
 def peaks():
@@ -440,6 +490,7 @@ def main():
                 "h2d_bytes_per_step": out["h2d"], "d2h_bytes_per_step": out["d2h"]},
         "gpu_launches": out["launches_round"] * K,
         "clocks": out["clocks"], "device_flags": out["flags"],
+        "decode_control": control_line(wl, out["ms"] / K, out["dec_ms"]),
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_rate(wl, args.cpu_seconds)
@@ -459,7 +510,8 @@ def main():
             also[name] = {"us_per_round": round(r_s * 1e6, 2), "value": o2["tokens"] / (o2["ms"] / 1e3),
                           "unit": UNIT, "steps": sub.steps, "bytes_min": b2,
                           "round_roofline_frac": round(b2 / (pk["hbm_gbs"] * 1e9) / r_s, 4),
-                          "clocks": o2["clocks"], "device_flags": o2["flags"]}
+                          "clocks": o2["clocks"], "device_flags": o2["flags"],
+                          "decode_control": control_line(w2, o2["ms"] / sub.steps, o2["dec_ms"])}
             torch.cuda.empty_cache()
         line["also"] = also
     print(json.dumps(line))

@@ -191,7 +191,7 @@ evs_status evs_prefill(evs_handle* h, const int32_t* tokens, int32_t P);
  *   near_tie     [B] uint32 or NULL: 1 when a decision was within near_tie_tau of
  *                flipping (greedy top-2 logit gap < tau * rms(logits); |u q - p| < tau p;
  *                u * sum(r) within tau * sum(r) of an inverse-CDF boundary).
- * Writes the block's K/V rows, FIR inputs and every IIR state s_0..s_gamma into the
+ * Writes the block's K/V rows, FIR inputs and IIR scan inputs u_0..u_gamma into the
  * workspace for evs_slice_state. State itself is not modified.
  * EVS_ERR_CAPACITY if kv_len + gamma + 1 could exceed t_max. */
 evs_status evs_verify_block(evs_handle* h, const int32_t* tokens, const int32_t* anchor,
@@ -199,13 +199,34 @@ evs_status evs_verify_block(evs_handle* h, const int32_t* tokens, const int32_t*
                             int32_t* accepted_len, int32_t* correction, int32_t* best_cand,
                             uint32_t* near_tie);
 
-/* State slicing at the accepted index (Figure 1(d); Lemma 3), in place, no replay:
- * kv_len += k + 1 (for n_cand > 1 the chosen candidate's k+1 block K/V rows are first
- * copied into the cache), FIR tail <- the last L-1 inputs up to block position k, IIR
- * state <- s_k. accepted_len and best_cand are device int32 [B] (usually the outputs of
- * the verify; best_cand may be NULL when n_cand == 1). k stays on the device: nothing is
- * read back. EVS_ERR_STATE if no verify was enqueued since the last slice or prefill. */
+/* State slicing at the accepted index (Figure 1(d); Lemma 3), in place, no replay of the
+ * forward: kv_len += k + 1 (for n_cand > 1 the chosen candidate's k+1 block K/V rows are
+ * first copied into the cache), FIR tail <- the last L-1 inputs up to block position k, IIR
+ * state <- s_k (k+1 steps of the diagonal recurrence from the pre-round state over the kept
+ * scan inputs, the same operations as the verify's scan). accepted_len and best_cand are
+ * device int32 [B] (usually the outputs of the verify; best_cand may be NULL when
+ * n_cand == 1). k stays on the device: nothing is read back. EVS_ERR_STATE if no verify was
+ * enqueued since the last slice, prefill, decode step or import. */
 evs_status evs_slice_state(evs_handle* h, const int32_t* accepted_len, const int32_t* best_cand);
+
+/* One step of plain autoregressive decoding: the target's native token-by-token loop that
+ * block verification is measured against (EvSpark summary, Interpretation: the
+ * identity-drafter control is reported as a multiple of native throughput). Every
+ * sequence consumes one token and its state advances in place (the K/V row is appended,
+ * the FIR tail shifts, the IIR state takes one step), then the next token is drawn from
+ * softmax(logits / temperature) of the new position: the argmax, lowest id on ties
+ * (greedy mode), or the inverse CDF at u[b] over ascending ids (sampling mode). Uses the
+ * verify's kernels with one row per sequence.
+ *   tokens    device int32 [B]: the token each sequence consumes.
+ *   uniforms  device fp32 [B] in [0, 1) (sampling mode; NULL in greedy mode).
+ *   next      device int32 [B]: the drawn next token. It may alias tokens (the draw is
+ *             written after every read of tokens, in stream order).
+ *   near_tie  device uint32 [B] or NULL: 1 when the draw was within near_tie_tau of
+ *             flipping (same tests as evs_verify_block).
+ * The step's logits are left in EVS_BUF_LOGITS rows [0, B). EVS_ERR_INVALID_ARG for a
+ * missing pointer, EVS_ERR_CAPACITY if kv_len + 1 could exceed t_max. */
+evs_status evs_decode_step(evs_handle* h, const int32_t* tokens, const float* uniforms, int32_t* next,
+                           uint32_t* near_tie);
 
 /* Copy a caller state into the handle (import) or the handle's state out (export).
  * Enqueued copies; export writes kv_len to the host view after synchronising the

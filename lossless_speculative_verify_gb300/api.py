@@ -121,6 +121,7 @@ class Verifier:
         B, Cn = cfg.batch, cfg.n_cand
         z = lambda n: torch.zeros(n, dtype=torch.int32, device=self.device)
         self.k, self.corr, self.cand, self.tie = z(B), z(B), z(B), z(B)
+        self.next, self.next_tie = z(B), z(B)
         self.kinds = [cfg.layer_kind[i] for i in range(cfg.n_layers)]
         self.params = [cfg.layer_param[i] for i in range(cfg.n_layers)]
 
@@ -139,6 +140,12 @@ class Verifier:
         k = self.k if k is None else k
         cand = self.cand if cand is None else cand
         L.check(self.lib.evs_slice_state(self.h, _vp(k), _vp(cand)), "evs_slice_state")
+
+    def decode(self, tokens, u=None, out=None):
+        """One native decode step: consume tokens [B], return (next [B], near_tie [B])."""
+        nxt, tie = out if out is not None else (self.next, self.next_tie)
+        L.check(self.lib.evs_decode_step(self.h, _vp(tokens), _vp(u), _vp(nxt), _vp(tie)), "evs_decode_step")
+        return nxt, tie
 
     def reset(self):
         L.check(self.lib.evs_reset(self.h), "evs_reset")

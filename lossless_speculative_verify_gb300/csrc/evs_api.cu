@@ -491,6 +491,22 @@ evs_status evs_verify_block(evs_handle* h, const int32_t* tokens, const int32_t*
     return after_launch(h);
 }
 
+evs_status evs_decode_step(evs_handle* h, const int32_t* tokens, const float* uniforms, int32_t* next,
+                           uint32_t* near_tie) {
+    if (!h || !tokens || !next) return EVS_ERR_INVALID_ARG;
+    if (h->cfg.mode == EVS_MODE_SAMPLING && !uniforms) return EVS_ERR_INVALID_ARG;
+    h->launches = 0;
+    if (h->kv_hi + 1 > h->cfg.t_max) return EVS_ERR_CAPACITY;
+    const int B = h->cfg.batch;
+    evs::Pass p{B, 1, 1, B, 1, 1};   // one committed position per sequence
+    run_layers(h, tokens, 1, nullptr, p, true);
+    evs::launch_advance(h, 1);
+    evs::launch_pick(h, uniforms, next, near_tie);
+    h->kv_hi += 1;
+    h->verified = 0;
+    return after_launch(h);
+}
+
 evs_status evs_slice_state(evs_handle* h, const int32_t* accepted_len, const int32_t* best_cand) {
     if (!h || !accepted_len) return EVS_ERR_INVALID_ARG;
     if (h->cfg.n_cand > 1 && !best_cand) return EVS_ERR_INVALID_ARG;

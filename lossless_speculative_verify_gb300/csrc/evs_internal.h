@@ -147,6 +147,7 @@ void launch_attention(evs_handle* h, int layer, const Pass& p);
 void launch_accept(evs_handle* h, const int32_t* tokens, const float* q, const float* u,
                    int32_t* acc, int32_t* corr, int32_t* cand, uint32_t* tie);
 void launch_slice(evs_handle* h, const int32_t* k, const int32_t* cand);
+void launch_pick(evs_handle* h, const float* u, int32_t* next, uint32_t* tie);
 void launch_advance(evs_handle* h, int T);
 
 }  // namespace evs

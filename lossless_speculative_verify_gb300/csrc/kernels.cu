@@ -1114,6 +1114,31 @@ void launch_accept(evs_handle* h, const int32_t* tokens, const float* q, const f
     prof_end(h, EVS_K_ACCEPT);
 }
 
+// The next-token draw of a decode step: the acceptance kernel over one candidate of one
+// position with no drafts (gamma 0), so it returns the argmax or the inverse-CDF draw at
+// u[b] of the position's distribution. The per-candidate words and k (always 0) land in
+// the handle's candidate scratch.
+void launch_pick(evs_handle* h, const float* u, int32_t* next, uint32_t* tie) {
+    prof_begin(h, EVS_K_ACCEPT);
+    const evs_config& c = h->cfg;
+    const int V = c.vocab;
+    const float inv_t = 1.0f / c.temperature;
+#define EVS_PICK(VPT)                                                                             \
+    launch_k(h, accept_kernel<VPT>, dim3(c.batch), dim3(ACC_THREADS), 0, h->logits, V, 1, 1, 0, c.mode, inv_t, \
+        c.near_tie_tau, (const int32_t*)nullptr, (const float*)nullptr, u, h->cand_k, h->cand_corr,            \
+        h->cand_tie, h->cand_k, next, (int32_t*)nullptr, tie, h->flags)
+    switch (V / ACC_THREADS) {
+        case 1: EVS_PICK(1); break;
+        case 2: EVS_PICK(2); break;
+        case 4: EVS_PICK(4); break;
+        case 8: EVS_PICK(8); break;
+        default: EVS_PICK(16); break;
+    }
+#undef EVS_PICK
+    h->launches++;
+    prof_end(h, EVS_K_ACCEPT);
+}
+
 void launch_slice(evs_handle* h, const int32_t* k, const int32_t* cand) {
     prof_begin(h, EVS_K_SLICE);
     const evs_config& c = h->cfg;

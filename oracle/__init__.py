@@ -26,13 +26,14 @@ design notes of the repository.
 
 Modules: ``model`` (token-by-token decode and an independent block-form forward),
 ``accept`` (greedy and rejection-sampling acceptance), ``verify`` (one round: block of
-steps, acceptance, snapshot at k).
+steps, acceptance, snapshot at k; and one step of native decoding).
 """
 from .model import Target, SeqState
 from .accept import (softmax_t, greedy_accept, sampling_accept, inverse_cdf, residual,
                      select_candidate)
-from .verify import verify_round, prefill, RoundResult, block_pass, accept_block, commit
+from .verify import (verify_round, prefill, RoundResult, block_pass, accept_block, commit, decode_step,
+                     pick_next)
 
 __all__ = ["Target", "SeqState", "softmax_t", "greedy_accept", "sampling_accept",
            "inverse_cdf", "residual", "select_candidate", "verify_round", "prefill",
-           "RoundResult", "block_pass", "accept_block", "commit"]
+           "RoundResult", "block_pass", "accept_block", "commit", "decode_step", "pick_next"]

@@ -7,6 +7,11 @@ and return the snapshot at the accepted index k: the state after consuming the a
 k drafts, with the readable KV length advanced by k+1 (EvSpark summary, Figure 1(c)-(d)).
 Nothing is recomputed after acceptance.
 
+Native decoding (``decode_step``), the baseline the block method is compared with (the
+identity-drafter control of the EvSpark summary, Interpretation, is a multiple of native
+throughput): one token per sequence, and the next token drawn from the new position's
+softmax(logits / T) by argmax or by inverse CDF at one uniform.
+
 With several candidates per sequence, each is verified from the same pre-round state with
 its own q and uniforms; the candidate with the largest k is committed (lowest index on
 ties), together with its block K/V rows, FIR tail and IIR state.
@@ -17,7 +22,8 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from .accept import greedy_accept, sampling_accept, select_candidate, softmax_t
+from .accept import (_cdf_tie, _gap_tie, greedy_accept, inverse_cdf, sampling_accept, select_candidate,
+                     softmax_t)
 
 
 @dataclass
@@ -127,3 +133,31 @@ def verify_round(target, states, tokens, q=None, u=None, mode="greedy", temperat
     commit(states, bp, k, cand)
     return RoundResult(logits=bp["logits"], k_c=k_c, corr_c=corr_c, tie_c=tie_c, k=k, corr=corr,
                        cand=cand, tie=tie, traces=bp["traces"])
+
+
+def pick_next(logits, u=None, mode="greedy", temperature=1.0, tau=0.0):
+    """The next token of native decoding from each sequence's logits [B, V]: the argmax
+    (lowest id on ties) in greedy mode, the inverse CDF of softmax(logits / T) at u[b] in
+    sampling mode. Returns next [B] and the near-tie flags [B] (the same tests as the
+    acceptance rule's)."""
+    logits = np.asarray(logits, np.float64)
+    B = logits.shape[0]
+    nxt = np.zeros(B, np.int64)
+    tie = np.zeros(B, bool)
+    for b in range(B):
+        if mode == "greedy":
+            nxt[b] = int(np.argmax(logits[b]))
+            tie[b] = _gap_tie(logits[b], tau)
+        else:
+            p = softmax_t(logits[b], temperature)
+            nxt[b] = inverse_cdf(p, float(u[b]))
+            tie[b] = _cdf_tie(p, float(u[b]), tau)
+    return nxt, tie
+
+
+def decode_step(target, states, tokens, u=None, mode="greedy", temperature=1.0, tau=0.0):
+    """One step of native decoding: sequence b consumes tokens[b] (its state advances in
+    place) and draws its next token. Returns logits [B, V], next [B], near-tie flags [B]."""
+    logits = np.stack([target.step(st, int(x)) for st, x in zip(states, tokens)])
+    nxt, tie = pick_next(logits, u, mode, temperature, tau)
+    return logits, nxt, tie

@@ -251,6 +251,49 @@ def test_greedy_identity_drafter_accepts_all_and_wrong_first_draft_rejects():
     assert r.k[0] == 0 and r.corr[0] == first
 
 
+def _decode_chain(tgt, st, anchor, n, mode, us=None):
+    toks, logits = [anchor], []
+    for i in range(n):
+        lg, nxt, _ = oracle.decode_step(tgt, [st], [toks[-1]], None if us is None else [us[i]], mode)
+        logits.append(lg[0])
+        toks.append(int(nxt[0]))
+    return toks, np.array(logits)
+
+
+@pytest.mark.parametrize("mode", ["greedy", "sampling"])
+def test_native_decode_chain_is_the_identity_drafter_round(mode):
+    """Native decoding against block verification: gamma+1 decode steps from a state give
+    the drafts of an identity drafter (greedy: the argmax chain; sampling: drafts drawn
+    from p itself, proposed with q = p), which a verify round accepts in full; its bonus is
+    the decode's next token for the same last uniform, and the sliced state is the state
+    after the decode steps."""
+    wl = tiny_wl()
+    tgt, st = _prefilled(wl, 9)
+    rng = np.random.default_rng(11)
+    us = rng.random(wl.gamma + 1)
+    dec = st.clone()
+    toks, logits = _decode_chain(tgt, dec, 67, wl.gamma + 1, mode, us)
+    q = oracle.softmax_t(logits[:wl.gamma], wl.temperature)[None, None]
+    u = np.concatenate([rng.random(wl.gamma), us[wl.gamma:]])[None, None]
+    ver = st.clone()
+    r = oracle.verify_round(tgt, [ver], np.array(toks[:-1])[None, None], q, u, mode, wl.temperature)
+    assert r.k[0] == wl.gamma and r.corr[0] == toks[-1]
+    _assert_same_state(ver, dec, tol=1e-12)
+
+
+def test_native_decode_sampling_draws_by_inverse_cdf():
+    """The sampled next token: over a fine grid of uniforms, each id is drawn for a share
+    of the grid equal to its target probability (to the grid's resolution)."""
+    rng = np.random.default_rng(5)
+    lg = rng.normal(size=(1, 16)) * 2
+    p = scipy.special.softmax(lg[0] / 0.7)
+    grid = (np.arange(20000) + 0.5) / 20000
+    ids = np.array([oracle.pick_next(lg, [g], "sampling", 0.7)[0][0] for g in grid])
+    freq = np.bincount(ids, minlength=16) / len(grid)
+    np.testing.assert_allclose(freq, p, atol=1.0 / len(grid) + 1e-12)
+    assert oracle.pick_next(lg, None, "greedy")[0][0] == int(np.argmax(lg[0]))
+
+
 def test_greedy_tie_goes_to_lowest_id():
     p = np.array([[0.1, 0.3, 0.3, 0.3], [0.25] * 4])
     k, corr, _ = oracle.greedy_accept(p, [2])
