@@ -212,7 +212,8 @@ def run_evs(args, wl, rank, world, light=False):
     K, W = args.steps, args.warmup
     P, T = wl.prefix_len, wl.block
     n_prof = min(K, 8)
-    rounds = W + 2 * K + 2 * n_prof + 2
+    n_abl = min(K, 8)                               # rounds of the slice / replay ablation
+    rounds = W + 2 * K + 2 * n_prof + 2 * n_abl + 2
     dec_steps = W + K + 2                           # native decode steps of the control leg
     t_max = (P + rounds * T + dec_steps + 255) // 256 * 256
     weights = gen_weights(wl)
@@ -300,9 +301,12 @@ def run_evs(args, wl, rank, world, light=False):
     ms = sum(a.elapsed_time(b) for a, b in evs)
     tokens = int(tok_acc.sum().item())
     clk = clocks.stop() if clocks is not None else None
+    abl = replay_ablation(ver, s, wl, lambda i: load_inputs(i % rounds, devin), buf, r, n_abl)
+    r += 2 * n_abl
     dec_ms = None if args.no_decode else decode_control(args, ver, s, flush, wl, K, W)
     if light:
-        return dict(ms=ms, tokens=tokens, clocks=clk, flags=ver.flags(), graph=graph is not None, dec_ms=dec_ms)
+        return dict(ms=ms, tokens=tokens, clocks=clk, flags=ver.flags(), graph=graph is not None, dec_ms=dec_ms,
+                    ablation=abl)
     # end-to-end through the public API: pinned host inputs in, accepted length and
     # correction out, every step
     e2e_ms = 0.0
@@ -359,7 +363,40 @@ def run_evs(args, wl, rank, world, light=False):
     ms, e2e_ms, tokens, e2e_tokens = aggregate(ms, e2e_ms, tokens, e2e_tokens, dev)
     return dict(ms=ms, tokens=tokens, e2e_ms=e2e_ms, e2e_tokens=e2e_tokens, h2d=h2d, d2h=d2h,
                 prof=prof, n_prof=n_prof, prof_mode=prof_mode, launches_round=launches_round, clocks=clk,
-                flags=flags, graph=graph is not None, dec_ms=dec_ms)
+                flags=flags, graph=graph is not None, dec_ms=dec_ms, ablation=abl)
+
+
+def replay_ablation(ver, s, wl, load, buf, r0, n):
+    """State recovery after a verify, two ways, on the same rounds (one sequence only): the
+    slice, and the replay ablation (k read back, then a second committed forward over the
+    accepted tokens). Each is bracketed by events on the stream after an eager verify; the
+    replay's bracket includes the host round trip for k. Returns mean µs of each."""
+    import torch
+    if wl.batch != 1:
+        return None
+    anc = torch.empty_like(ver.corr)
+    out = {}
+    for leg in ("slice", "replay"):
+        tot, acc = 0.0, 0
+        for i in range(n):
+            with torch.cuda.stream(s):
+                load(r0 + i + (n if leg == "replay" else 0))
+                anc.copy_(ver.corr)
+                ver.verify(buf["tokens"], buf.get("q"), buf.get("u"), anchor=anc)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(s)
+                if leg == "slice":
+                    ver.slice()
+                else:
+                    ver.replay(buf["tokens"], anchor=anc)
+                b.record(s)
+            s.synchronize()
+            tot += a.elapsed_time(b)
+            acc += int(ver.k.item()) + 1
+        out[f"{leg}_us"] = round(tot / n * 1e3, 2)
+        out[f"{leg}_tokens_per_round"] = acc / n
+    out["replay_over_slice"] = out["replay_us"] / out["slice_us"]
+    return out
 
 
 def decode_control(args, ver, s, flush, wl, K, W):
@@ -491,6 +528,7 @@ def main():
         "gpu_launches": out["launches_round"] * K,
         "clocks": out["clocks"], "device_flags": out["flags"],
         "decode_control": control_line(wl, out["ms"] / K, out["dec_ms"]),
+        "recovery_ablation": out["ablation"],
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_rate(wl, args.cpu_seconds)
@@ -511,7 +549,8 @@ def main():
                           "unit": UNIT, "steps": sub.steps, "bytes_min": b2,
                           "round_roofline_frac": round(b2 / (pk["hbm_gbs"] * 1e9) / r_s, 4),
                           "clocks": o2["clocks"], "device_flags": o2["flags"],
-                          "decode_control": control_line(w2, o2["ms"] / sub.steps, o2["dec_ms"])}
+                          "decode_control": control_line(w2, o2["ms"] / sub.steps, o2["dec_ms"]),
+                          "recovery_ablation": o2["ablation"]}
             torch.cuda.empty_cache()
         line["also"] = also
     print(json.dumps(line))

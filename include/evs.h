@@ -209,6 +209,20 @@ evs_status evs_verify_block(evs_handle* h, const int32_t* tokens, const int32_t*
  * enqueued since the last slice, prefill, decode step or import. */
 evs_status evs_slice_state(evs_handle* h, const int32_t* accepted_len, const int32_t* best_cand);
 
+/* Replay-based recovery, the ablation that slicing replaces (EvSpark summary,
+ * Interpretation: slicing against a second target forward over the accepted prefix). After
+ * evs_verify_block, k and the committed candidate are read back to the host (the stream is
+ * synchronised), then a committed forward runs over that candidate's accepted tokens
+ * [anchor, d_1..d_k] from the pre-round state, as a prefill does. The state it leaves equals
+ * the one evs_slice_state leaves, up to rounding. One sequence only (batch == 1): the
+ * accepted lengths of different sequences differ.
+ *   tokens, anchor  as given to the verify (anchor may be NULL).
+ *   accepted_len, best_cand  the verify's outputs (device; best_cand NULL when n_cand == 1).
+ * EVS_ERR_STATE without a preceding verify; EVS_ERR_INVALID_ARG if batch > 1, a pointer is
+ * missing, or k / the candidate read back is out of range. */
+evs_status evs_replay_state(evs_handle* h, const int32_t* tokens, const int32_t* anchor,
+                            const int32_t* accepted_len, const int32_t* best_cand);
+
 /* One step of plain autoregressive decoding: the target's native token-by-token loop that
  * block verification is measured against (EvSpark summary, Interpretation: the
  * identity-drafter control is reported as a multiple of native throughput). Every

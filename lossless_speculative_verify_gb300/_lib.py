@@ -23,7 +23,7 @@ FLAG_KV_OVERFLOW, FLAG_BAD_K, FLAG_EMPTY_RESIDUAL, FLAG_BAD_TOKEN, FLAG_TIMEOUT 
 
 EXPORTED = (
     "evs_workspace_bytes", "evs_create", "evs_destroy", "evs_set_stream", "evs_reset",
-    "evs_prefill", "evs_verify_block", "evs_slice_state", "evs_decode_step", "evs_import_state",
+    "evs_prefill", "evs_verify_block", "evs_slice_state", "evs_replay_state", "evs_decode_step", "evs_import_state",
     "evs_export_state", "evs_debug_buffer", "evs_device_flags", "evs_last_launch_count",
     "evs_status_str", "evs_profile_enable", "evs_profile_read", "evs_debug_projection",
     "evs_projection_noalloc",
@@ -93,6 +93,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.evs_verify_block.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.evs_slice_state.restype = C.c_int
     lib.evs_slice_state.argtypes = [vp, vp, vp]
+    lib.evs_replay_state.restype = C.c_int
+    lib.evs_replay_state.argtypes = [vp, vp, vp, vp, vp]
     lib.evs_decode_step.restype = C.c_int
     lib.evs_decode_step.argtypes = [vp, vp, vp, vp, vp]
     lib.evs_import_state.restype = C.c_int

@@ -141,6 +141,13 @@ class Verifier:
         cand = self.cand if cand is None else cand
         L.check(self.lib.evs_slice_state(self.h, _vp(k), _vp(cand)), "evs_slice_state")
 
+    def replay(self, tokens, k=None, cand=None, anchor=None):
+        """Replay-based recovery after a verify (ablation of slice; one sequence only)."""
+        k = self.k if k is None else k
+        cand = self.cand if cand is None else cand
+        L.check(self.lib.evs_replay_state(self.h, _vp(tokens), _vp(anchor), _vp(k), _vp(cand)),
+                "evs_replay_state")
+
     def decode(self, tokens, u=None, out=None):
         """One native decode step: consume tokens [B], return (next [B], near_tie [B])."""
         nxt, tie = out if out is not None else (self.next, self.next_tie)

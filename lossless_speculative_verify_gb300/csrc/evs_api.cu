@@ -491,6 +491,35 @@ evs_status evs_verify_block(evs_handle* h, const int32_t* tokens, const int32_t*
     return after_launch(h);
 }
 
+evs_status evs_replay_state(evs_handle* h, const int32_t* tokens, const int32_t* anchor,
+                            const int32_t* accepted_len, const int32_t* best_cand) {
+    if (!h || !tokens || !accepted_len) return EVS_ERR_INVALID_ARG;
+    const evs_config& c = h->cfg;
+    if (c.batch != 1 || (c.n_cand > 1 && !best_cand)) return EVS_ERR_INVALID_ARG;
+    if (!h->verified) return EVS_ERR_STATE;
+    h->launches = 0;
+    int32_t kc[2] = {0, 0};
+    if (cudaMemcpyAsync(&kc[0], accepted_len, 4, cudaMemcpyDeviceToHost, h->stream) != cudaSuccess ||
+        (best_cand && cudaMemcpyAsync(&kc[1], best_cand, 4, cudaMemcpyDeviceToHost, h->stream) != cudaSuccess) ||
+        cudaStreamSynchronize(h->stream) != cudaSuccess)
+        return EVS_ERR_CUDA;
+    const int k = kc[0], cand = c.n_cand > 1 ? kc[1] : 0, T = c.gamma + 1;
+    if (k < 0 || k > c.gamma || cand < 0 || cand >= c.n_cand) return EVS_ERR_INVALID_ARG;
+    // the accepted tokens of the candidate, consumed prefill_chunk at a time from the
+    // pre-round state (the verify left the state itself untouched)
+    const int32_t* acc = tokens + (size_t)cand * T;
+    for (int off = 0; off <= k; off += c.prefill_chunk) {
+        const int n = std::min(c.prefill_chunk, k + 1 - off);
+        evs::Pass p{1, 1, n, n, 1, 1};
+        run_layers(h, acc + off, T, off == 0 ? anchor : nullptr, p, false);
+        evs::launch_advance(h, n);
+    }
+    h->kv_hi += T;
+    if (h->kv_hi > c.t_max) h->kv_hi = c.t_max;
+    h->verified = 0;
+    return after_launch(h);
+}
+
 evs_status evs_decode_step(evs_handle* h, const int32_t* tokens, const float* uniforms, int32_t* next,
                            uint32_t* near_tie) {
     if (!h || !tokens || !next) return EVS_ERR_INVALID_ARG;
