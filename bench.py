@@ -154,7 +154,7 @@ def oracle_rate(wl, seconds, rounds_from=0):
     while True:
         rnd = gen_round(wl, rounds_from + rounds, anchor=anchor)
         res = oracle.verify_round(tgt, states, rnd["tokens"], rnd["q"], rnd["u"], wl.mode,
-                                  wl.temperature)
+                                  wl.temperature, rule=wl.cand_rule)
         anchor = res.corr
         tokens += int((res.k + 1).sum())
         rounds += 1
@@ -221,7 +221,7 @@ def run_evs(args, wl, rank, world, light=False):
     dw = DeviceWeights(layers, weights, wl.dtype, dev)
     del weights
     cfg = make_config(wl.d, layers, wl.head_dim, wl.gamma, wl.batch, wl.n_cand, t_max,
-                      wl.prefill_chunk, wl.dtype, wl.mode, wl.temperature, 0.0, wl.vocab)
+                      wl.prefill_chunk, wl.dtype, wl.mode, wl.temperature, 0.0, wl.vocab, wl.cand_rule)
     s = torch.cuda.Stream(dev)
     ver = Verifier(cfg, dw, dev, stream=s)
     # synthetic pre-round state: O(1) FIR / IIR states from the seeded generator, KV rows

@@ -63,6 +63,15 @@ typedef enum {
 enum { EVS_LAYER_FIR = 0, EVS_LAYER_IIR = 1, EVS_LAYER_ATTN = 2 };
 enum { EVS_DTYPE_F32 = 0, EVS_DTYPE_BF16 = 1 };
 enum { EVS_MODE_GREEDY = 0, EVS_MODE_SAMPLING = 1 };
+/* How several candidate blocks per sequence are verified under sampling (greedy commits
+ * the candidate with the most accepted drafts under both, which is exact there):
+ *   EVS_CAND_RECURSIVE   lossless: rejection sampling applied recursively across the
+ *                        candidates that share the accepted prefix (a token tree with equal
+ *                        prefixes merged); the output follows the target distribution.
+ *   EVS_CAND_MAX_ACCEPT  each candidate tested alone with its own uniforms, the one with
+ *                        the most accepted drafts committed (lowest index on ties); not
+ *                        distribution-preserving in general. */
+enum { EVS_CAND_RECURSIVE = 0, EVS_CAND_MAX_ACCEPT = 1 };
 
 /* Bits of the device flag word (evs_device_flags). */
 enum {
@@ -92,6 +101,7 @@ typedef struct {
     int32_t mode;                         /* EVS_MODE_*                                 */
     float temperature;                    /* p = softmax(logits / temperature), > 0     */
     float near_tie_tau;                   /* relative threshold of the near-tie flags   */
+    int32_t cand_rule;                    /* EVS_CAND_* (n_cand > 1, sampling)          */
 } evs_config;
 
 typedef struct {

@@ -17,6 +17,7 @@ EVS_OK, EVS_ERR_INVALID_ARG, EVS_ERR_CAPACITY, EVS_ERR_STATE, EVS_ERR_CUDA = ran
 LAYER_FIR, LAYER_IIR, LAYER_ATTN = 0, 1, 2
 DTYPE_F32, DTYPE_BF16 = 0, 1
 MODE_GREEDY, MODE_SAMPLING = 0, 1
+CAND_RECURSIVE, CAND_MAX_ACCEPT = 0, 1
 FLAG_KV_OVERFLOW, FLAG_BAD_K, FLAG_EMPTY_RESIDUAL, FLAG_BAD_TOKEN, FLAG_TIMEOUT = 1, 2, 4, 8, 16
 (BUF_LOGITS, BUF_FIR_STAGE, BUF_IIR_U, BUF_K_CACHE, BUF_V_CACHE, BUF_K_SIDE, BUF_V_SIDE,
  BUF_KV_LEN, BUF_FIR_TAIL, BUF_IIR_STATE, BUF_CAND_K, BUF_CAND_CORR) = range(12)
@@ -38,7 +39,7 @@ class Config(C.Structure):
                 ("head_dim", C.c_int32), ("gamma", C.c_int32), ("batch", C.c_int32),
                 ("n_cand", C.c_int32), ("t_max", C.c_int32), ("prefill_chunk", C.c_int32),
                 ("dtype", C.c_int32), ("mode", C.c_int32), ("temperature", C.c_float),
-                ("near_tie_tau", C.c_float)]
+                ("near_tie_tau", C.c_float), ("cand_rule", C.c_int32)]
 
 
 class LayerWeights(C.Structure):

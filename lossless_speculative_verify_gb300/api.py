@@ -34,8 +34,9 @@ class _DeviceArray:
 
 
 def make_config(d, layers, head_dim, gamma, batch, n_cand, t_max, prefill_chunk, dtype, mode,
-                temperature=1.0, near_tie_tau=0.0, vocab=512) -> L.Config:
-    """layers: sequence of (kind, param) with kind in {"fir", "iir", "attn"}."""
+                temperature=1.0, near_tie_tau=0.0, vocab=512, cand_rule="recursive") -> L.Config:
+    """layers: sequence of (kind, param) with kind in {"fir", "iir", "attn"}; cand_rule:
+    "recursive" (lossless) or "max_accept", for several candidates under sampling."""
     cfg = L.Config()
     cfg.d, cfg.vocab, cfg.n_layers = d, vocab, len(layers)
     for i, (kind, param) in enumerate(layers):
@@ -46,6 +47,7 @@ def make_config(d, layers, head_dim, gamma, batch, n_cand, t_max, prefill_chunk,
     cfg.dtype = L.DTYPE_BF16 if dtype == "bf16" else L.DTYPE_F32
     cfg.mode = L.MODE_SAMPLING if mode == "sampling" else L.MODE_GREEDY
     cfg.temperature, cfg.near_tie_tau = temperature, near_tie_tau
+    cfg.cand_rule = {"recursive": L.CAND_RECURSIVE, "max_accept": L.CAND_MAX_ACCEPT}[cand_rule]
     return cfg
 
 

@@ -98,6 +98,7 @@ bool valid_config(const evs_config* c) {
     if (c->t_max < 1 || c->t_max > (1 << 21)) return false;
     if (c->dtype != EVS_DTYPE_F32 && c->dtype != EVS_DTYPE_BF16) return false;
     if (c->mode != EVS_MODE_GREEDY && c->mode != EVS_MODE_SAMPLING) return false;
+    if (c->cand_rule != EVS_CAND_RECURSIVE && c->cand_rule != EVS_CAND_MAX_ACCEPT) return false;
     if (!(c->temperature > 0.f) || !(c->near_tie_tau >= 0.f)) return false;
     return true;
 }

@@ -710,9 +710,124 @@ __device__ int inverse_cdf(float (&r)[VPT], float u, float tau, bool& tie, float
     return (first != 0x7fffffff) ? first : lastpos;
 }
 
+// p = softmax(row * inv_temp) over ids tid*VPT + t, normalised; l keeps the raw logits and
+// sq their per-thread sum of squares.
+template <int VPT>
+__device__ void softmax_row(const float* __restrict__ row, float inv_temp, float (&l)[VPT], float (&pr)[VPT],
+                            float& sq, float* redf) {
+    float mx = -INFINITY;
+    sq = 0.f;
+#pragma unroll
+    for (int t = 0; t < VPT; ++t) {
+        l[t] = row[threadIdx.x * VPT + t];
+        mx = fmaxf(mx, l[t] * inv_temp);
+        sq += l[t] * l[t];
+    }
+    mx = block_max(mx, redf);
+    float se = 0.f;
+#pragma unroll
+    for (int t = 0; t < VPT; ++t) { pr[t] = __expf(l[t] * inv_temp - mx); se += pr[t]; }
+    se = block_sum(se, redf);
+    const float inv_se = 1.f / se;
+#pragma unroll
+    for (int t = 0; t < VPT; ++t) pr[t] *= inv_se;
+}
+
+// Several candidate blocks of sequence b under sampling, losslessly: rejection sampling
+// applied recursively across the candidates that share the accepted path (a token tree with
+// equal prefixes merged). At depth j the alive candidates are tried in index order against
+// r (the lowest alive candidate's p at position j, then renormalised residuals
+// max(0, r - q_c) after each rejection); an accepted draft x keeps alive the candidates whose
+// draft j+1 is x. If all are rejected the correction is the inverse-CDF draw from r, after
+// gamma acceptances the bonus from p at the path's end, both at u[lead][gamma]; the lowest
+// alive candidate is committed. cand_k holds each candidate's drafts on the path, cand_corr
+// the correction for the committed candidate and -1 for the others.
+template <int VPT>
+__device__ void accept_recursive(int b, const float* __restrict__ logits, int V, int C, int Tb, int gamma,
+                                 float inv_temp, float tau, const int32_t* __restrict__ tokens,
+                                 const float* __restrict__ qprob, const float* __restrict__ unif,
+                                 int32_t* __restrict__ cand_k, int32_t* __restrict__ cand_corr,
+                                 uint32_t* __restrict__ cand_tie, int32_t* __restrict__ out_k,
+                                 int32_t* __restrict__ out_corr, int32_t* __restrict__ out_cand,
+                                 uint32_t* __restrict__ out_tie, uint32_t* __restrict__ flags, float* redf,
+                                 int* redi, float* pd_sh) {
+    const int tid = threadIdx.x;
+    auto draft = [&](int c, int j) {   // draft j+1 of candidate c, clamped like the embedding
+        const int t = tokens[((size_t)b * C + c) * Tb + j + 1];
+        return t < 0 ? 0 : (t >= V ? V - 1 : t);
+    };
+    uint32_t alive = C >= 32 ? 0xffffffffu : ((1u << C) - 1u);
+    int k = gamma, corr = 0, lead = 0;
+    bool tie = false;
+    for (int j = 0; j <= gamma; ++j) {
+        lead = __ffs(alive) - 1;
+        float l[VPT], pr[VPT], sq;
+        softmax_row<VPT>(logits + (((size_t)b * C + lead) * Tb + j) * V, inv_temp, l, pr, sq, redf);
+        int x_acc = -1;
+        for (int c = lead; j < gamma && c < C; ++c) {
+            if (!((alive >> c) & 1u)) continue;
+            const size_t bc = (size_t)b * C + c;
+            const int x = draft(c, j);
+            const float* qrow = qprob + (bc * gamma + j) * V;
+            if (x / VPT == tid) {
+#pragma unroll
+                for (int t = 0; t < VPT; ++t)
+                    if (tid * VPT + t == x) *pd_sh = pr[t];
+            }
+            __syncthreads();
+            const float pd = *pd_sh;
+            __syncthreads();
+            const float lhs = unif[bc * Tb + j] * qrow[x];
+            if (tau > 0.f && fabsf(lhs - pd) < tau * pd) tie = true;
+            if (lhs < pd) {
+                x_acc = x;
+                break;
+            }
+            float r[VPT], rs = 0.f;
+#pragma unroll
+            for (int t = 0; t < VPT; ++t) {
+                r[t] = fmaxf(pr[t] - qrow[tid * VPT + t], 0.f);
+                rs += r[t];
+            }
+            rs = block_sum(rs, redf);
+            if (rs > 0.f) {
+                const float inv = 1.f / rs;
+#pragma unroll
+                for (int t = 0; t < VPT; ++t) pr[t] = r[t] * inv;
+            } else if (tid == 0) {
+                atomicOr(flags, (uint32_t)EVS_FLAG_EMPTY_RESIDUAL);
+            }
+        }
+        if (x_acc < 0) {
+            k = j;
+            corr = inverse_cdf<VPT>(pr, unif[((size_t)b * C + lead) * Tb + gamma], tau, tie, redf, redi);
+            break;
+        }
+        uint32_t keep = 0;
+        for (int c = lead; c < C; ++c)
+            if (((alive >> c) & 1u) && draft(c, j) == x_acc) keep |= 1u << c;
+        if (tid == 0)
+            for (int c = 0; c < C; ++c)
+                if (((alive & ~keep) >> c) & 1u) cand_k[(size_t)b * C + c] = j;
+        alive = keep;
+    }
+    if (tid == 0) {
+        for (int c = 0; c < C; ++c) {
+            const size_t bc = (size_t)b * C + c;
+            if ((alive >> c) & 1u) cand_k[bc] = k;
+            cand_corr[bc] = c == lead ? corr : -1;
+            cand_tie[bc] = tie ? 1u : 0u;
+        }
+        out_k[b] = k;
+        out_corr[b] = corr;
+        if (out_cand) out_cand[b] = lead;
+        if (out_tie) out_tie[b] = tie ? 1u : 0u;
+    }
+}
+
 template <int VPT>
 __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(
-    const float* __restrict__ logits, int V, int C, int Tb, int gamma, int mode, float inv_temp,
+    const float* __restrict__ logits, int V, int C, int Tb, int gamma, int mode, int rule, float inv_temp,
     float tau, const int32_t* __restrict__ tokens, const float* __restrict__ qprob,
     const float* __restrict__ unif, int32_t* __restrict__ cand_k, int32_t* __restrict__ cand_corr,
     uint32_t* __restrict__ cand_tie, int32_t* __restrict__ out_k, int32_t* __restrict__ out_corr,
@@ -725,6 +840,11 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_kernel(
     __shared__ float pd_sh;
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
+    if (mode == EVS_MODE_SAMPLING && C > 1 && rule == EVS_CAND_RECURSIVE) {
+        accept_recursive<VPT>(b, logits, V, C, Tb, gamma, inv_temp, tau, tokens, qprob, unif, cand_k, cand_corr,
+                              cand_tie, out_k, out_corr, out_cand, out_tie, flags, redf, redi, &pd_sh);
+        return;
+    }
     int best_c = 0, best_k = -1, best_corr = 0;
     uint32_t any_tie = 0;
     for (int c = 0; c < C; ++c) {
@@ -1100,8 +1220,8 @@ void launch_accept(evs_handle* h, const int32_t* tokens, const float* q, const f
     const int Tb = c.gamma + 1;
 #define EVS_ACC(VPT)                                                                              \
     launch_k(h, accept_kernel<VPT>, dim3(c.batch), dim3(ACC_THREADS), 0, h->logits, V, c.n_cand, Tb, c.gamma,   \
-        c.mode, inv_t, c.near_tie_tau, tokens, q, u, h->cand_k, h->cand_corr, h->cand_tie, acc, corr, \
-        cand, tie, h->flags)
+        c.mode, c.cand_rule, inv_t, c.near_tie_tau, tokens, q, u, h->cand_k, h->cand_corr, h->cand_tie, acc, \
+        corr, cand, tie, h->flags)
     switch (V / ACC_THREADS) {
         case 1: EVS_ACC(1); break;
         case 2: EVS_ACC(2); break;
@@ -1124,7 +1244,7 @@ void launch_pick(evs_handle* h, const float* u, int32_t* next, uint32_t* tie) {
     const int V = c.vocab;
     const float inv_t = 1.0f / c.temperature;
 #define EVS_PICK(VPT)                                                                             \
-    launch_k(h, accept_kernel<VPT>, dim3(c.batch), dim3(ACC_THREADS), 0, h->logits, V, 1, 1, 0, c.mode, inv_t, \
+    launch_k(h, accept_kernel<VPT>, dim3(c.batch), dim3(ACC_THREADS), 0, h->logits, V, 1, 1, 0, c.mode, 0, inv_t, \
         c.near_tie_tau, (const int32_t*)nullptr, (const float*)nullptr, u, h->cand_k, h->cand_corr,            \
         h->cand_tie, h->cand_k, next, (int32_t*)nullptr, tie, h->flags)
     switch (V / ACC_THREADS) {

@@ -30,10 +30,10 @@ steps, acceptance, snapshot at k; and one step of native decoding).
 """
 from .model import Target, SeqState
 from .accept import (softmax_t, greedy_accept, sampling_accept, inverse_cdf, residual,
-                     select_candidate)
+                     select_candidate, multi_candidate_accept)
 from .verify import (verify_round, prefill, RoundResult, block_pass, accept_block, commit, decode_step,
                      pick_next)
 
 __all__ = ["Target", "SeqState", "softmax_t", "greedy_accept", "sampling_accept",
            "inverse_cdf", "residual", "select_candidate", "verify_round", "prefill",
-           "RoundResult", "block_pass", "accept_block", "commit", "decode_step", "pick_next"]
+           "RoundResult", "block_pass", "accept_block", "commit", "decode_step", "pick_next", "multi_candidate_accept"]

@@ -12,6 +12,10 @@ u_j uniform in [0, 1); at the first rejection the correction is drawn from
 max(0, p_j - q_j) renormalised; if every draft is accepted the bonus is drawn from
 p_{gamma+1}. Both draws use the last uniform, u_gamma, by inverse CDF over ascending ids.
 
+Several candidates per sequence: either each candidate is tested alone and the one with
+the most accepted drafts is committed (``select_candidate``; exact for greedy, not for
+sampling), or the lossless recursive rule of ``multi_candidate_accept``.
+
 Indexing: ``p_rows[i]`` is the target distribution computed at block position i (after
 consuming the anchor and drafts 1..i), i.e. the distribution for draft i+1; ``q_rows[j]``
 and ``drafts[j]`` are draft j+1's proposal distribution and token.
@@ -75,8 +79,9 @@ def greedy_accept(p_rows, drafts, logits=None, tau=0.0):
     return k, corr, tie
 
 
-def sampling_accept(p_rows, q_rows, drafts, u, tau=0.0):
-    """Returns (k, correction, near_tie, residual_was_empty)."""
+def sampling_accept(p_rows, q_rows, drafts, u, tau=0.0, trace=None):
+    """Returns (k, correction, near_tie, residual_was_empty). ``trace``, when a list,
+    receives ("test", j, accepted) and ("draw", gamma, token) in order."""
     g = len(drafts)
     tie = False
     for j in range(g):
@@ -85,6 +90,8 @@ def sampling_accept(p_rows, q_rows, drafts, u, tau=0.0):
         lhs = float(u[j]) * qj
         if tau > 0 and abs(lhs - pj) < tau * pj:
             tie = True
+        if trace is not None:
+            trace.append(("test", j, lhs < pj))
         if lhs < pj:
             continue
         r = residual(p_rows[j], q_rows[j])
@@ -92,10 +99,81 @@ def sampling_accept(p_rows, q_rows, drafts, u, tau=0.0):
         if empty:
             r = np.asarray(p_rows[j], np.float64)
         tie = tie or _cdf_tie(r, float(u[g]), tau)
-        return j, inverse_cdf(r, float(u[g])), tie, empty
+        tok = inverse_cdf(r, float(u[g]))
+        if trace is not None:
+            trace.append(("draw", g, tok))
+        return j, tok, tie, empty
     r = np.asarray(p_rows[g], np.float64)
     tie = tie or _cdf_tie(r, float(u[g]), tau)
-    return g, inverse_cdf(r, float(u[g])), tie, False
+    tok = inverse_cdf(r, float(u[g]))
+    if trace is not None:
+        trace.append(("draw", g, tok))
+    return g, tok, tie, False
+
+
+def multi_candidate_accept(p_rows, q_rows, drafts, u, tau=0.0, trace=None):
+    """Lossless verification of several candidate blocks of one sequence: rejection
+    sampling applied recursively across the candidates, which form a token tree whose
+    equal prefixes are merged (the multi-candidate / tree verification the EvSpark summary
+    cites as related work; ReaDy appendix D.2 for the single-chain rule it extends).
+
+    p_rows [C][gamma+1][V]: each candidate's target distributions along its own block;
+    q_rows [C][gamma][V], drafts [C][gamma], u [C][gamma+1].
+
+    At depth j the alive candidates (whose drafts 1..j equal the accepted path; all of them
+    at j = 0) are tried in index order against the current distribution r (p at the path's
+    position j, taken from the lowest alive candidate): draft x of candidate c is accepted
+    iff u[c][j] q_c(x) < r(x); after a rejection r becomes max(0, r - q_c) renormalised
+    (left unchanged, and the round marked, if that has no mass). On acceptance the alive
+    set shrinks to the candidates whose draft j+1 is x. If every alive candidate is
+    rejected the correction is drawn from r, and after gamma acceptances the bonus from p
+    at the end of the path, both by inverse CDF at u[lead][gamma] (lead: the lowest alive
+    index), which is the committed candidate.
+
+    Returns (k, correction, committed candidate, near_tie, residual_was_empty, depth [C]):
+    depth[c] is how many of candidate c's drafts lie on the accepted path. ``trace``, when
+    a list, receives ("test", c, j, accepted) and ("draw", c, gamma, token) in order."""
+    C, g = len(drafts), len(drafts[0])
+    alive = list(range(C))
+    depth = np.zeros(C, np.int64)
+    tie = empty = False
+    for j in range(g + 1):
+        lead = alive[0]
+        r = np.asarray(p_rows[lead][j], np.float64)
+        x_acc = None
+        if j < g:
+            for c in alive:
+                x = int(drafts[c][j])
+                qc = np.asarray(q_rows[c][j], np.float64)
+                rn = r / r.sum()
+                lhs = float(u[c][j]) * qc[x]
+                if tau > 0 and abs(lhs - rn[x]) < tau * rn[x]:
+                    tie = True
+                ok = lhs < rn[x]
+                if trace is not None:
+                    trace.append(("test", c, j, ok))
+                if ok:
+                    x_acc = x
+                    break
+                res = residual(rn, qc)
+                if res.sum() > 0:
+                    r = res
+                else:
+                    empty = True
+        if x_acc is None:
+            depth[alive] = j
+            ug = float(u[lead][g])
+            tie = tie or _cdf_tie(r, ug, tau)
+            tok = inverse_cdf(r, ug)
+            if trace is not None:
+                trace.append(("draw", lead, g, tok))
+            return j, tok, lead, tie, empty, depth
+        keep = [c for c in alive if int(drafts[c][j]) == x_acc]
+        for c in alive:
+            if c not in keep:
+                depth[c] = j
+        alive = keep
+    raise AssertionError("unreachable")
 
 
 def select_candidate(ks):

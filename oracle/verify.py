@@ -12,9 +12,12 @@ identity-drafter control of the EvSpark summary, Interpretation, is a multiple o
 throughput): one token per sequence, and the next token drawn from the new position's
 softmax(logits / T) by argmax or by inverse CDF at one uniform.
 
-With several candidates per sequence, each is verified from the same pre-round state with
-its own q and uniforms; the candidate with the largest k is committed (lowest index on
-ties), together with its block K/V rows, FIR tail and IIR state.
+With several candidates per sequence, each block is computed from the same pre-round state;
+under sampling the lossless recursive rule (``multi_candidate_accept``) picks the accepted
+path and the committed candidate, or, by choice, each candidate is tested alone with its own
+q and uniforms and the one with the largest k is committed (lowest index on ties; the rule
+for greedy either way). The committed candidate's block K/V rows, FIR tail and IIR state are
+kept.
 """
 from __future__ import annotations
 
@@ -22,8 +25,8 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from .accept import (_cdf_tie, _gap_tie, greedy_accept, inverse_cdf, sampling_accept, select_candidate,
-                     softmax_t)
+from .accept import (_cdf_tie, _gap_tie, greedy_accept, inverse_cdf, multi_candidate_accept, sampling_accept,
+                     select_candidate, softmax_t)
 
 
 @dataclass
@@ -83,14 +86,34 @@ def block_pass(target, states, tokens):
     return out
 
 
-def accept_block(logits, tokens, q=None, u=None, mode="greedy", temperature=1.0, tau=0.0):
+def accept_block(logits, tokens, q=None, u=None, mode="greedy", temperature=1.0, tau=0.0,
+                 rule="recursive"):
     """Acceptance for every (sequence, candidate) of a block from its logits [B, C, T, V];
-    returns k_c, corr_c, tie_c [B, C] and the committed k, corr, cand, tie [B]."""
+    returns k_c, corr_c, tie_c [B, C] and the committed k, corr, cand, tie [B].
+
+    Sampling with several candidates follows ``rule``: "recursive" (lossless, recursive
+    rejection across the candidates; k_c is then each candidate's depth on the accepted
+    path and corr_c the correction for the committed candidate, -1 for the others) or
+    "max_accept" (each candidate alone, the most accepted drafts committed). Greedy is the
+    same under both."""
     tokens = np.asarray(tokens)
     B, C, T = tokens.shape
     k_c = np.zeros((B, C), np.int64)
     corr_c = np.zeros((B, C), np.int64)
     tie_c = np.zeros((B, C), bool)
+    if mode == "sampling" and C > 1 and rule == "recursive":
+        k = np.zeros(B, np.int64)
+        corr = np.zeros(B, np.int64)
+        cand = np.zeros(B, np.int64)
+        for b in range(B):
+            p = [softmax_t(np.asarray(logits[b, c], np.float64), temperature) for c in range(C)]
+            kb, cb, lead, tie, _, depth = multi_candidate_accept(p, q[b], tokens[b, :, 1:], u[b], tau)
+            k[b], corr[b], cand[b] = kb, cb, lead
+            k_c[b] = depth
+            corr_c[b] = -1
+            corr_c[b, lead] = cb
+            tie_c[b] = tie
+        return k_c, corr_c, tie_c, k, corr, cand, tie_c.any(axis=1)
     for b in range(B):
         for c in range(C):
             lg = np.asarray(logits[b, c], np.float64)
@@ -124,12 +147,12 @@ def commit(states, bp, k, cand):
 
 
 def verify_round(target, states, tokens, q=None, u=None, mode="greedy", temperature=1.0,
-                 tau=0.0) -> RoundResult:
+                 tau=0.0, rule="recursive") -> RoundResult:
     """``states`` is a list (one ``SeqState`` per sequence), updated in place to the
     sliced state. tokens int [B, C, gamma+1]; q [B, C, gamma, V]; u [B, C, gamma+1]."""
     bp = block_pass(target, states, tokens)
     k_c, corr_c, tie_c, k, corr, cand, tie = accept_block(bp["logits"], tokens, q, u, mode,
-                                                          temperature, tau)
+                                                          temperature, tau, rule)
     commit(states, bp, k, cand)
     return RoundResult(logits=bp["logits"], k_c=k_c, corr_c=corr_c, tie_c=tie_c, k=k, corr=corr,
                        cand=cand, tie=tie, traces=bp["traces"])

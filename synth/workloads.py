@@ -46,6 +46,7 @@ class Workload:
     q_alpha: float = 1.0  # Dirichlet concentration of the draft distribution over ACGT
     prefix_kind: str = "uniform"  # "uniform" or "markov3"
     prefill_chunk: int = 64
+    cand_rule: str = "recursive"  # several candidates under sampling: "recursive" or "max_accept"
 
     # ---- derived sizes -------------------------------------------------------------
     @property

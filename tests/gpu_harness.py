@@ -29,7 +29,7 @@ def make_verifier(wl, weights, t_max, near_tie_tau=None):
     from lossless_speculative_verify_gb300 import DeviceWeights, Verifier, make_config
     tau = TAU[wl.dtype] if near_tie_tau is None else near_tie_tau
     cfg = make_config(wl.d, layer_list(wl), wl.head_dim, wl.gamma, wl.batch, wl.n_cand, t_max,
-                      wl.prefill_chunk, wl.dtype, wl.mode, wl.temperature, tau, wl.vocab)
+                      wl.prefill_chunk, wl.dtype, wl.mode, wl.temperature, tau, wl.vocab, wl.cand_rule)
     dw = DeviceWeights(layer_list(wl), weights, wl.dtype)
     return Verifier(cfg, dw)
 
@@ -186,7 +186,7 @@ class Pair:
         states = [self.states[b] for b in sq]
         bp = oracle.block_pass(self.tgt, states, sub(rnd["tokens"]))
         own = oracle.accept_block(bp["logits"], sub(rnd["tokens"]), sub(rnd["q"]), sub(rnd["u"]),
-                                  wl.mode, wl.temperature, TAU[wl.dtype])
+                                  wl.mode, wl.temperature, TAU[wl.dtype], wl.cand_rule)
         k, corr, cand, tie = self.ver.verify(toks, q, u)
         self.round_launches = self.ver.launches          # kernels of the verify call
         torch.cuda.synchronize()
@@ -195,14 +195,20 @@ class Pair:
         B, C, T, V = wl.batch, wl.n_cand, wl.block, wl.vocab
         glog = self.ver.buffer(0, -1, torch.float32, (B, C, T, V)).cpu().numpy()[sq]
         kern = oracle.accept_block(glog, sub(rnd["tokens"]), sub(rnd["q"]), sub(rnd["u"]), wl.mode,
-                                   wl.temperature, TAU["f32"])
+                                   wl.temperature, TAU["f32"], wl.cand_rule)
         gk, gc, gcand = k.cpu().numpy()[sq], corr.cpu().numpy()[sq], cand.cpu().numpy()[sq]
         gcand = gcand if C > 1 else np.zeros_like(gk)
+        if C > 1:   # per-candidate words: accepted drafts (or depth on the path), corrections
+            gkc = self.ver.buffer(10, -1, torch.int32, (B, C)).cpu().numpy()[sq]
+            gcc = self.ver.buffer(11, -1, torch.int32, (B, C)).cpu().numpy()[sq]
         for i in range(len(sq)):
             if kern[6][i]:
                 continue
             assert gk[i] == kern[3][i] and gc[i] == kern[4][i] and gcand[i] == kern[5][i], \
                 (sq[i], gk, gc, gcand, kern[3:6])
+            if C > 1:
+                np.testing.assert_array_equal(gkc[i], kern[0][i])
+                np.testing.assert_array_equal(gcc[i], kern[1][i])
         oracle.commit(states, bp, gk, gcand)
         self.ver.slice(k, cand)
         self.round_launches += self.ver.launches         # plus the slice

@@ -139,6 +139,27 @@ def test_multi_candidate_fp32():
     assert _lockstep(pair, 3, first_round=2) <= 1
 
 
+def _shared_prefixes(pair, rnd):
+    """Candidates 1 and 2 copy candidate 0's first draft, candidate 2 also its second, so
+    the accepted path keeps several candidates alive."""
+    toks = rnd["tokens"].copy()
+    toks[:, 1, 1] = toks[:, 0, 1]
+    toks[:, 2, 1:3] = toks[:, 0, 1:3]
+    return toks
+
+
+@pytest.mark.parametrize("rule", ["recursive", "max_accept"])
+def test_multi_candidate_sampling_fp32(rule):
+    """Several candidates under sampling, both rules: committed k, correction and candidate
+    and every candidate's words exact against the oracle (fp32, also its own fp64
+    decisions), over rounds where candidates share drafts."""
+    wl = get_workload("tiny_d64_fp32").replace(batch=2, n_cand=3, gamma=5, mode="sampling", q_alpha=0.5,
+                                               cand_rule=rule)
+    pair = Pair(wl)
+    pair.import_synthetic(48)
+    assert _lockstep(pair, 8, drafts=_shared_prefixes) <= 2
+
+
 def test_multi_candidate_sampling_bf16():
     wl = get_workload("tiny_d64_fp32").replace(
         d=256, dtype="bf16", head_dim=128, batch=2, n_cand=4, gamma=6, mode="sampling",

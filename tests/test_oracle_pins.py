@@ -4,6 +4,7 @@ Each check below compares the oracle with a library routine, a closed form, an i
 or a value printed on the EvSpark pages (tests/golden), so that a dropped term, wrong
 index, sign or transposed operand in the oracle fails at least one of them.
 """
+import itertools
 import json
 import os
 
@@ -414,6 +415,128 @@ def test_sampling_round_is_exact_by_enumeration():
             for k2, p2 in sub[key[0]].items():
                 two[key[0], k2[0]] += pr * p2
     np.testing.assert_allclose(two, tab["p0"][:, None] * tab["p"], atol=1e-12)
+
+
+class _U:
+    """Uniforms u[c][j] of a round from a dict of values (0 where none is given)."""
+
+    def __init__(self, vals, c=None):
+        self.vals, self.c = vals, c
+
+    def __getitem__(self, i):
+        return _U(self.vals, i) if self.c is None else self.vals.get((self.c, i), 0.0)
+
+
+def _explore_law(fn, V):
+    """Exact law of fn(u, trace) over independent uniforms u[c][j] ~ U[0,1), for a fn that
+    uses each uniform at most once: in a threshold test, traced as ("test", c, j, accepted)
+    and accepted below some threshold, or in a draw, traced as ("draw", c, j, token) with
+    the token non-decreasing in u. The first uniform not yet confined to an interval is
+    split where its decision changes (found by bisection) and each part explored."""
+    law = {}
+
+    def decision(vals, cj):
+        tr = []
+        fn(_U(vals), tr)
+        return next(e for e in tr if (e[1], e[2]) == cj)[3]
+
+    def explore(fixed, w):
+        vals = {cj: 0.5 * (lo + hi) for cj, (lo, hi) in fixed.items()}
+        tr = []
+        out = fn(_U(vals), tr)
+        free = next((e for e in tr if (e[1], e[2]) not in fixed), None)
+        if free is None:
+            law[out] = law.get(out, 0.0) + w
+            return
+        kind, cj = free[0], (free[1], free[2])
+        at = lambda x: {**vals, cj: x}
+        if kind == "test":
+            a = _bisect(lambda x: decision(at(x), cj)) if decision(at(0.0), cj) else 0.0
+            parts = [(0.0, a), (a, 1.0)]
+        else:
+            edges = [0.0] + [_bisect(lambda x, v=v: decision(at(x), cj) <= v) for v in range(V)]
+            parts = list(zip(edges[:-1], edges[1:]))
+        for lo, hi in parts:
+            if hi > lo:
+                explore({**fixed, cj: (lo, hi)}, w * (hi - lo))
+
+    explore({}, 1.0)
+    return law
+
+
+def _multi_round_law(tab, ctx, gamma, C, rule):
+    """Exact law of the tokens one round with C independently drafted candidate blocks
+    emits from context ctx (table target, order-1 Markov)."""
+    V = tab["p"].shape[0]
+    p_of = lambda a: tab["p0"] if a is None else tab["p"][a]
+    q_of = lambda a: tab["q0"] if a is None else tab["q"][a]
+    law = {}
+    chains = []
+
+    def rec(d, w):
+        if len(d) == gamma:
+            chains.append((d, w))
+            return
+        prev = d[-1] if d else ctx
+        for x in range(V):
+            rec(d + [x], w * q_of(prev)[x])
+
+    rec([], 1.0)
+    for combo in itertools.product(chains, repeat=C):
+        drafts = [d for d, _ in combo]
+        w = float(np.prod([wc for _, wc in combo]))
+        p_rows = [[p_of(a) for a in [ctx] + d] for d in drafts]
+        q_rows = [[q_of(a) for a in [ctx] + d[:-1]] for d in drafts]
+
+        def fn(u, tr):
+            if rule == "recursive":
+                k, corr, c, *_ = oracle.multi_candidate_accept(p_rows, q_rows, drafts, u, trace=tr)
+                return tuple(drafts[c][:k]) + (corr,)
+            res = []
+            for c in range(C):
+                t = []
+                k, corr, _, _ = oracle.sampling_accept(p_rows[c], q_rows[c], drafts[c], u[c], trace=t)
+                tr.extend((e[0], c) + e[1:] for e in t)
+                res.append((k, corr))
+            c = max(range(C), key=lambda i: (res[i][0], -i))
+            return tuple(drafts[c][:res[c][0]]) + (res[c][1],)
+
+        for key, pr in _explore_law(fn, V).items():
+            law[key] = law.get(key, 0.0) + w * pr
+    return law
+
+
+def _first_two(law_of, V):
+    law = law_of(None)
+    first = np.zeros(V)
+    for key, pr in law.items():
+        first[key[0]] += pr
+    sub = {a: law_of(a) for a in range(V)}
+    two = np.zeros((V, V))
+    for key, pr in law.items():
+        if len(key) >= 2:
+            two[key[0], key[1]] += pr
+        else:
+            for k2, p2 in sub[key[0]].items():
+                two[key[0], k2[0]] += pr * p2
+    return sum(law.values()), first, two
+
+
+def test_multi_candidate_recursive_rule_is_exact_by_enumeration():
+    """Two candidate blocks drafted independently (V=3, gamma=2): with recursive rejection
+    across the candidates the first emitted token has law p(. | ctx) and the first two have
+    law p(a | ctx) p(b | a), to 1e-12; committing the candidate with the most accepted
+    drafts instead is measurably biased on the same target."""
+    from synth import gen_table_target
+    V, gamma, C = 3, 2, 2
+    tab = gen_table_target(V, seed=13)
+    tot, first, two = _first_two(lambda a: _multi_round_law(tab, a, gamma, C, "recursive"), V)
+    assert abs(tot - 1.0) < 1e-12
+    np.testing.assert_allclose(first, tab["p0"], atol=1e-12)
+    np.testing.assert_allclose(two, tab["p0"][:, None] * tab["p"], atol=1e-12)
+    tot, first, two = _first_two(lambda a: _multi_round_law(tab, a, gamma, C, "max_accept"), V)
+    assert abs(tot - 1.0) < 1e-12
+    assert np.abs(two - tab["p0"][:, None] * tab["p"]).max() > 1e-3
 
 
 def test_sampling_round_chi_square():
