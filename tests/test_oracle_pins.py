@@ -561,6 +561,39 @@ def test_sampling_round_chi_square():
     assert chisquare(counts, tab["p0"] * n).pvalue > 1e-3
 
 
+def test_multi_candidate_recursive_chi_square():
+    """Seeded sampler check of the recursive multi-candidate rule at a size the enumeration
+    cannot reach (4 candidates, V=6, gamma=3): first emitted token of 20000 rounds vs p,
+    and the second token given the first among rounds that emit two (alpha = 1e-3)."""
+    from scipy.stats import chisquare
+    from synth import gen_table_target
+    V, gamma, C, n = 6, 3, 4, 20000
+    tab = gen_table_target(V, seed=14)
+    rng = np.random.Generator(np.random.PCG64(101))
+    first = np.zeros(V)
+    second = np.zeros((V, V))
+    for _ in range(n):
+        drafts = []
+        for _ in range(C):
+            d, prev = [], None
+            for _ in range(gamma):
+                prev = int(rng.choice(V, p=tab["q0"] if prev is None else tab["q"][prev]))
+                d.append(prev)
+            drafts.append(d)
+        p_rows = [[tab["p0"]] + [tab["p"][a] for a in d] for d in drafts]
+        q_rows = [[tab["q0"]] + [tab["q"][a] for a in d[:-1]] for d in drafts]
+        k, corr, c, *_ = oracle.multi_candidate_accept(p_rows, q_rows, drafts, rng.random((C, gamma + 1)))
+        out = drafts[c][:k] + [corr]
+        first[out[0]] += 1
+        if len(out) >= 2:
+            second[out[0], out[1]] += 1
+    assert chisquare(first, tab["p0"] * n).pvalue > 1e-3
+    for a in range(V):
+        m = second[a].sum()
+        if m >= 500:
+            assert chisquare(second[a], tab["p"][a] * m).pvalue > 1e-3
+
+
 def test_multi_candidate_selects_longest_lowest_index():
     assert oracle.select_candidate([1, 3, 3, 0]) == 1
     assert oracle.select_candidate([0, 0, 0, 0]) == 0
