@@ -5,7 +5,7 @@ the accepted prefix is the longest run of drafts equal to the target's argmax; t
 target's argmax at the first mismatch (or after the last draft, the bonus) becomes the
 correction. Ties in argmax go to the lowest token id.
 
-Rejection sampling (EvSpark, Figure 1(c) "sampled correction"; ReaDy, appendix D.2,
+Rejection sampling (EvSpark, Figure 1(c): the correction may be sampled; ReaDy, appendix D.2,
 the target distribution is preserved): draft d_j is accepted with probability
 min(1, p_j(d_j) / q_j(d_j)), realised as the strict test u_j * q_j(d_j) < p_j(d_j) with
 u_j uniform in [0, 1); at the first rejection the correction is drawn from
