@@ -146,8 +146,10 @@ enum {
     EVS_BUF_KV_LEN = 7,     /* [B] int32                                                  */
     EVS_BUF_FIR_TAIL = 8,   /* layer: [B][L-1][d] fp32                                    */
     EVS_BUF_IIR_STATE = 9,  /* layer: [B][d][N][2] fp32                                   */
-    EVS_BUF_CAND_K = 10,    /* [B][C] int32 accepted drafts per candidate, last verify    */
-    EVS_BUF_CAND_CORR = 11  /* [B][C] int32 correction per candidate, last verify         */
+    EVS_BUF_CAND_K = 10,    /* [B][C] int32 accepted drafts per candidate, last verify
+                               (EVS_CAND_RECURSIVE sampling: drafts on the accepted path) */
+    EVS_BUF_CAND_CORR = 11  /* [B][C] int32 correction per candidate, last verify
+                               (EVS_CAND_RECURSIVE sampling: -1 but for the committed one) */
 };
 
 typedef struct {
@@ -196,8 +198,9 @@ evs_status evs_prefill(evs_handle* h, const int32_t* tokens, int32_t P);
  * Outputs (device, written by the enqueued kernels):
  *   accepted_len [B] int32: k, accepted drafts of the committed candidate (0..gamma).
  *   correction   [B] int32: next anchor (correction at the first rejection, or bonus).
- *   best_cand    [B] int32 or NULL: committed candidate (most accepted drafts, lowest
- *                index on ties); required when n_cand > 1.
+ *   best_cand    [B] int32 or NULL: committed candidate (see EVS_CAND_*: the lowest
+ *                candidate on the accepted path, or the most accepted drafts with the
+ *                lowest index on ties); required when n_cand > 1.
  *   near_tie     [B] uint32 or NULL: 1 when a decision was within near_tie_tau of
  *                flipping (greedy top-2 logit gap < tau * rms(logits); |u q - p| < tau p;
  *                u * sum(r) within tau * sum(r) of an inverse-CDF boundary).
