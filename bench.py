@@ -44,6 +44,7 @@ def parse():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-also", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-decode", action="store_true", help="skip the native-decode control leg")
+    ap.add_argument("--no-ablation", action="store_true", help="skip the slice / replay ablation leg")
     ap.add_argument("--prefix", type=int, default=None,
                     help="cached tokens per sequence instead of the workload's (small profiling "
                          "cases; the workload name then carries the override)")
@@ -301,7 +302,8 @@ def run_evs(args, wl, rank, world, light=False):
     ms = sum(a.elapsed_time(b) for a, b in evs)
     tokens = int(tok_acc.sum().item())
     clk = clocks.stop() if clocks is not None else None
-    abl = replay_ablation(ver, s, wl, lambda i: load_inputs(i % rounds, devin), buf, r, n_abl)
+    abl = None if args.no_ablation else replay_ablation(ver, s, wl, lambda i: load_inputs(i % rounds, devin), buf,
+                                                          r, n_abl)
     r += 2 * n_abl
     dec_ms = None if args.no_decode else decode_control(args, ver, s, flush, wl, K, W)
     if light:
