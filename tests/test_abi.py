@@ -52,6 +52,30 @@ def test_workspace_bytes_and_validation(lib):
     assert workspace_bytes(_cfg(gamma=0)) == 0
     assert workspace_bytes(_cfg(layers=[("iir", 3)])) == 0     # poles not a power of two
     assert workspace_bytes(_cfg(vocab=500)) == 0
+    bad_rule = _cfg()
+    bad_rule.cand_rule = 2
+    assert workspace_bytes(bad_rule) == 0                      # unknown candidate rule
+
+
+def test_iir_workspace_keeps_inputs_not_states(lib):
+    """A verify keeps the IIR scan inputs ([B][C][gamma+1][d] fp32) for slicing, not every
+    state: more poles grow the workspace by the carried state [B][d][N] complex only."""
+    from lossless_speculative_verify_gb300 import workspace_bytes
+    al = lambda x: (x + 255) // 256 * 256
+    for B, C, g in [(1, 1, 6), (2, 3, 5)]:
+        kw = dict(batch=B, n_cand=C, gamma=g, d=64)
+        w1 = workspace_bytes(_cfg(layers=[("iir", 1)], **kw))
+        w16 = workspace_bytes(_cfg(layers=[("iir", 16)], **kw))
+        assert w16 - w1 == al(B * 64 * 16 * 8) - al(B * 64 * 1 * 8)
+
+
+def test_entry_points_reject_a_null_handle(lib):
+    from lossless_speculative_verify_gb300 import _lib
+    null = ctypes.c_void_p()
+    assert lib.evs_decode_step(null, null, null, null, null) == _lib.EVS_ERR_INVALID_ARG
+    assert lib.evs_replay_state(null, null, null, null, null) == _lib.EVS_ERR_INVALID_ARG
+    assert lib.evs_slice_state(null, null, null) == _lib.EVS_ERR_INVALID_ARG
+    assert lib.evs_verify_block(null, null, null, null, null, null, null, null, null) == _lib.EVS_ERR_INVALID_ARG
 
 
 def test_create_rejects_bad_arguments_on_the_host(lib):
