@@ -169,6 +169,18 @@ def test_multi_candidate_sampling_bf16():
     _lockstep(pair, 4)
 
 
+def test_multi_candidate_bf16_wide_block():
+    """112 block rows (4 sequences x 4 candidates x 7), more than the in-projection
+    epilogue's mixers take: the standalone FIR / IIR kernels run on 16 blocks, with
+    decisions and the sliced state against the oracle."""
+    wl = get_workload("tiny_d64_fp32").replace(
+        d=256, dtype="bf16", head_dim=128, batch=4, n_cand=4, gamma=6, mode="sampling",
+        layers=(LayerSpec("fir", 3), LayerSpec("iir", 16), LayerSpec("fir", 7), LayerSpec("attn", 2)))
+    pair = Pair(wl)
+    pair.import_synthetic(200)
+    _lockstep(pair, 3)
+
+
 def test_bf16_small_stack_sampling():
     wl = get_workload("d1024_l8_p8k_bf16").replace(d=256, head_dim=128, prefix_len=500,
         layers=(LayerSpec("fir", 3), LayerSpec("iir", 16), LayerSpec("fir", 3), LayerSpec("attn", 2)) * 2)
