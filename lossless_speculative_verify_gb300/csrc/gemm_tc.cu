@@ -44,6 +44,7 @@ constexpr int TC_A_BYTES = TC_BM * TC_BK * 2; // 16 KiB
 #define EVS_TC_MIN_KB 2        // fewest 64-wide k-blocks a split may stream
 #endif
 constexpr int TC_SMEM_BUDGET = EVS_TC_SMEM_KB * 1024;
+constexpr int TC_EXCLUSIVE_SMEM = 200 * 1024;   // dynamic shared memory of a CTA that needs its SM alone
 #ifndef EVS_TC_KBS
 #define EVS_TC_KBS 4          // 64-wide k-blocks per pipeline stage (longer contiguous row reads)
 #endif
@@ -683,9 +684,9 @@ int gemm_tc_init() {
     return dyn;
 }
 
-// Split K only as far as each CTA still streams at least 8 k-blocks (128 KiB of weights),
-// and no further than filling the 152 SMs once: past that the partial-sum round trip and
-// the per-CTA start-up cost more than the extra parallelism returns.
+// Split K only as far as each CTA still streams at least EVS_TC_MIN_KB k-blocks, and no
+// further than about two CTAs per SM: past that the partial-sum round trip and the per-CTA
+// start-up cost more than the extra parallelism returns.
 int tc_cta_target() { return EVS_TC_CTA_TARGET; }
 
 int tc_splits(int N, int K) {
@@ -731,6 +732,11 @@ static TcShape tc_shape(int M, int N, int K, size_t part_cap = (size_t)-1, int m
     t.ncols = 32;
     while (t.ncols < t.n_pad) t.ncols <<= 1;
     t.smem = (size_t)t.stages * t.kbs * kb_bytes + 1024 + (2 * t.stages + 1) * 8;
+    // a 512-column accumulator takes all of an SM's tensor memory. Such a CTA gets the SM to
+    // itself (more shared memory than leaves room for any other projection or attention
+    // CTA): otherwise a CTA could hold the columns while it waits on a cluster peer or on its
+    // predecessor kernel, with the CTA it waits for stuck in its own allocation.
+    if (t.ncols > 256) t.smem = std::max(t.smem, (size_t)TC_EXCLUSIVE_SMEM);
     // cluster reduction when the splits fit a portable cluster and the scratch holds every
     // partial tile of the launch
     t.cluster = allow_cluster && t.splits > 1 && t.splits <= 8 && (size_t)N * t.splits * M <= part_cap;
