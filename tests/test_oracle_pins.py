@@ -332,6 +332,26 @@ def test_acceptance_probability_is_min_one_p_over_q():
         assert abs(thr - min(1.0, pd / qd)) < 1e-15
 
 
+def test_inverse_cdf_boundaries_are_half_open():
+    """Inverse-transform sampling maps u in [F(v-1), F(v)) to id v, so a u exactly on F(v)
+    goes to the next id (exactly representable boundaries)."""
+    r = np.array([1.0, 1.0, 2.0])                     # F = 0.25, 0.5, 1.0
+    assert [oracle.inverse_cdf(r, u) for u in (0.0, 0.25, 0.375, 0.5, 0.75)] == [0, 1, 1, 2, 2]
+    p = np.array([[0.25, 0.25, 0.5], [0.25, 0.25, 0.5]])
+    assert oracle.pick_next(np.log(p[:1]), [0.25], "sampling")[0][0] == 1
+
+
+def test_acceptance_boundary_is_strict():
+    """Draft d is accepted iff u q(d) < p(d), u in [0, 1): the accepted set of u is
+    [0, p/q), so u exactly at p/q rejects (reading of the test at its measure-zero edge)."""
+    p = np.array([[0.25, 0.75], [0.5, 0.5]])
+    q = np.array([[0.5, 0.5]])
+    assert oracle.sampling_accept(p, q, [0], [0.5, 0.1])[0] == 0           # 0.5 * 0.5 == 0.25
+    assert oracle.sampling_accept(p, q, [0], [np.nextafter(0.5, 0), 0.1])[0] == 1
+    k, _, cand, *_ = oracle.multi_candidate_accept([p, p], [q, q], [[0], [1]], [[0.5, 0.1], [0.0, 0.1]])
+    assert k == 1 and cand == 1                    # first rejected at the edge, second accepted
+
+
 def test_inverse_cdf_interval_lengths_are_the_distribution():
     """Inverse-transform sampling: the u-interval mapped to id v has length r_v / sum r."""
     r = np.array([0.0, 0.3, 0.0, 0.05, 0.4, 0.25]) * 3.7
