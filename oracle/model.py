@@ -7,7 +7,7 @@ attention caches; EvSpark summary, Figure 1(d) and Interpretation paragraph 1):
   h <- E[x]
   per layer:  xh = h / sqrt(mean(h^2) + 1e-6)
     FIR-L   v = xh W_in;  y = sum_{j<L} w[:, j] * v_{t-j};  h += y W_out
-            state: the last L-1 inputs v (the "outer-FIR inputs" of Figure 1(d))
+            state: the last L-1 inputs v (the FIR inputs Figure 1(d) carries over)
     IIR-N   u = xh W_in;  s_t = lam * s_{t-1} + b * u_t  (N complex poles per channel)
             y = Re sum_n c_n s_{t,n};  h += y W_out;  state: s
     attn    q, k, v = xh W_q, xh W_k, xh W_v;  per head o = softmax(q K^T / sqrt(dh)) V
@@ -28,7 +28,8 @@ EPS = 1e-6
 
 
 def fir_step(tail, v, taps):
-    """One depthwise FIR step. tail [L-1, d] holds the previous inputs, oldest first;
+    """One depthwise FIR step (EvSpark summary, Figure 1(d): a finite window of the last L-1
+    inputs is the FIR state). tail [L-1, d] holds the previous inputs, oldest first;
     returns y = sum_j taps[:, j] * v_{t-j} and the new tail (the last L-1 inputs)."""
     Lf = taps.shape[1]
     window = np.vstack([tail, v[None]])          # v_{t-L+1} .. v_t
@@ -39,13 +40,15 @@ def fir_step(tail, v, taps):
 
 
 def iir_step(s, u, lam, b, c):
-    """One modal IIR step: s' = lam * s + b * u (per channel, N poles), y = Re sum_n c s'."""
+    """One modal IIR step (EvSpark summary, Figure 1(d): the modal state s is the IIR state):
+    s' = lam * s + b * u (per channel, N poles), y = Re sum_n c s'."""
     s_new = lam * s + b * u[:, None]
     return np.real(np.sum(c * s_new, axis=1)), s_new
 
 
 def attend(q, K, V):
-    """Single-query attention over rows [0, n) of K, V: softmax(K q / sqrt(dh)) V."""
+    """Single-query attention over rows [0, n) of K, V: softmax(K q / sqrt(dh)) V (EvSpark
+    summary, Figure 1(d): the query reads the readable KV prefix)."""
     K = np.asarray(K, np.float64)
     V = np.asarray(V, np.float64)
     sc = K @ q / np.sqrt(q.shape[-1])
@@ -93,7 +96,8 @@ class SeqState:
         return None
 
     def snapshot(self):
-        """Copy of the O(1) states; KV represented by its readable length only."""
+        """Copy of the O(1) states; KV represented by its readable length only (EvSpark
+        summary, Figure 1(d): slicing keeps the state at k and shortens the KV prefix)."""
         snap = []
         for L in self.layers:
             if L["kind"] == "fir":
@@ -178,7 +182,9 @@ class Target:
         return h / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + EPS)
 
     def step(self, st: SeqState, x: int, trace: list | None = None) -> np.ndarray:
-        """Consume token x: update ``st`` in place and return the next-token logits."""
+        """Consume token x: update ``st`` in place and return the next-token logits. This is
+        the definition every other form is checked against (sequential decode; EvSpark
+        summary, Interpretation paragraph 1, Lemmas 2 and 3)."""
         h = self.E[x].copy()
         for L, S in zip(self.layers, st.layers):
             xh = self.rmsnorm(h)
