@@ -304,19 +304,32 @@ evs_status evs_debug_projection(evs_handle* h, const void* X, int32_t x_rows, co
  * evs_debug_projection; split-K partial sums always go through the fixed array (never
  * through a thread-block cluster). X: device bf16 [x_rows][K] (x_rows >= M); W: device bf16
  * out-major [N][K]; Y: device fp32 [M][ldy]; stream: a cudaStream_t. Needs M <= 512,
- * N % 128 == 0, N <= 32768, K % 64 == 0.
- * Scratch: one fixed array of 8 MiB of fp32 partial sums (plus 256 counters) compiled
- * into the library, held on every GPU that loads it until the process exits. Shapes whose
- * split-K partial sums (splits x M x N floats) exceed 2^21 floats return EVS_ERR_CAPACITY.
- * The first call on a device looks up the array's device address and sets the kernel's
- * shared-memory limit for that device; make that first call before any stream capture.
+ * N % 128 == 0, K % 64 == 0.
+ * Scratch: one fixed array of 8 MiB of fp32 partial sums, 256 arrival counters and a flag
+ * word, compiled into the library and held on every GPU that loads it until the process
+ * exits. The K split is capped so that its partial sums (splits x M x N floats) fit 2^21
+ * floats (a shape that fits no split runs unsplit), so the only size limit is N <= 32768
+ * (one counter per 128-channel tile); wider N returns EVS_ERR_CAPACITY.
+ * The first call on a device (of this function or evs_projection_noalloc_flags) looks up
+ * the array's device address, sets the kernel's shared-memory limit for that device and
+ * clears the flag word; make that first call before any stream capture. The set-up is
+ * guarded, so host threads may make their first calls concurrently. A device reset
+ * (cudaDeviceReset) invalidates it: reload the library after one.
  * Every call reuses the same array and finds the previous call's contents there; the
  * counters are cleared on the stream at each call. Calls that overlap on the GPU (issued
  * on different streams, or from several host threads) race on it: order them on one
- * stream. EVS_ERR_INVALID_ARG for bad shapes or pointers, EVS_ERR_CUDA if a
- * CUDA call fails. */
+ * stream. A kernel that gives up a bounded wait sets EVS_FLAG_TIMEOUT in the array's flag
+ * word, and Y is then void; read the word with evs_projection_noalloc_flags.
+ * EVS_ERR_INVALID_ARG for bad shapes or pointers, EVS_ERR_CUDA if a CUDA call fails. */
 evs_status evs_projection_noalloc(const void* X, int32_t x_rows, const void* W, float* Y, int32_t M,
                                   int32_t N, int32_t K, int32_t ldy, int32_t accumulate, void* stream);
+
+/* Device status of evs_projection_noalloc on the current device: synchronises stream, then
+ * writes to *flags the EVS_FLAG_* bits (EVS_FLAG_TIMEOUT) that its calls have set since the
+ * word was last cleared, and clears it when clear != 0 (enqueued on stream). Allocates
+ * nothing. EVS_ERR_INVALID_ARG for a null flags pointer, EVS_ERR_CUDA if a CUDA call
+ * fails. */
+evs_status evs_projection_noalloc_flags(uint32_t* flags, int32_t clear, void* stream);
 
 /* Static description of a status code. */
 const char* evs_status_str(evs_status s);

@@ -27,7 +27,7 @@ EXPORTED = (
     "evs_prefill", "evs_verify_block", "evs_slice_state", "evs_replay_state", "evs_decode_step", "evs_import_state",
     "evs_export_state", "evs_debug_buffer", "evs_device_flags", "evs_last_launch_count",
     "evs_status_str", "evs_profile_enable", "evs_profile_read", "evs_debug_projection",
-    "evs_projection_noalloc",
+    "evs_projection_noalloc", "evs_projection_noalloc_flags",
 )
 KERNEL_KINDS = ("embed", "norm", "gemm", "fir", "iir", "kv_write", "attn", "attn_combine", "accept",
                 "slice", "advance")
@@ -116,6 +116,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.evs_debug_projection.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, i32, i32]
     lib.evs_projection_noalloc.restype = C.c_int
     lib.evs_projection_noalloc.argtypes = [vp, i32, vp, vp, i32, i32, i32, i32, i32, vp]
+    lib.evs_projection_noalloc_flags.restype = C.c_int
+    lib.evs_projection_noalloc_flags.argtypes = [C.POINTER(C.c_uint32), i32, vp]
     lib.evs_status_str.restype = C.c_char_p
     lib.evs_status_str.argtypes = [C.c_int]
     _lib = lib

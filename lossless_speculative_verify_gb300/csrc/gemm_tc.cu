@@ -18,6 +18,8 @@
 // their 32 TMEM lanes for the epilogue.
 #include <cudaTypedefs.h>
 
+#include <atomic>
+#include <mutex>
 #include <type_traits>
 
 #include "evs_common.cuh"
@@ -882,9 +884,36 @@ struct NoAllocScratch {
 static __device__ __align__(256) NoAllocScratch g_noalloc_scratch;
 
 // Per-device set-up results: the array's device address and the kernel's shared-memory
-// limit. Filled by the first call on each device.
-NoAllocScratch* g_noalloc_ptr[kNoAllocMaxDevices];
+// limit, filled once per device under the mutex (by the first call that finds them unset)
+// and published through the atomic pointer after the limit is written.
+std::mutex g_noalloc_mu;
+std::atomic<NoAllocScratch*> g_noalloc_ptr[kNoAllocMaxDevices];
 int g_noalloc_smem[kNoAllocMaxDevices];
+
+// The current device's scratch address (set-up on first use), or null with *st set.
+NoAllocScratch* noalloc_scratch(cudaStream_t s, evs_status* st, int* dev_out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) { *st = EVS_ERR_CUDA; return nullptr; }
+    if (dev < 0 || dev >= kNoAllocMaxDevices) { *st = EVS_ERR_INVALID_ARG; return nullptr; }
+    *dev_out = dev;
+    NoAllocScratch* p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+    if (p) return p;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    p = g_noalloc_ptr[dev].load(std::memory_order_relaxed);
+    if (p) return p;
+    // one-time set-up on this device (the device is current here): the array's address,
+    // the kernel's shared-memory opt-in, and a cleared flag word
+    if (cudaGetSymbolAddress((void**)&p, g_noalloc_scratch) != cudaSuccess || !p) {
+        *st = EVS_ERR_CUDA;
+        return nullptr;
+    }
+    const int smem_max = gemm_tc_init();
+    if (smem_max < 0) { *st = EVS_ERR_CUDA; return nullptr; }
+    if (cudaMemsetAsync(&p->flags, 0, sizeof(uint32_t), s) != cudaSuccess) { *st = EVS_ERR_CUDA; return nullptr; }
+    g_noalloc_smem[dev] = smem_max;
+    g_noalloc_ptr[dev].store(p, std::memory_order_release);
+    return p;
+}
 
 }  // namespace
 }  // namespace evs
@@ -893,30 +922,21 @@ extern "C" evs_status evs_projection_noalloc(const void* X, int32_t x_rows, cons
                                              int32_t N, int32_t K, int32_t ldy, int32_t accumulate,
                                              void* stream) {
     using namespace evs;
-    if (!X || !W || !Y || !gemm_tc_supported(M, N, K) || x_rows < M || ldy < N || N / TC_BM > kNoAllocCounters)
-        return EVS_ERR_INVALID_ARG;
+    if (!X || !W || !Y || !gemm_tc_supported(M, N, K) || x_rows < M || ldy < N) return EVS_ERR_INVALID_ARG;
+    if (N / TC_BM > kNoAllocCounters) return EVS_ERR_CAPACITY;   // more channel tiles than counters
+    cudaStream_t s = (cudaStream_t)stream;
+    evs_status st = EVS_OK;
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return EVS_ERR_CUDA;
-    if (dev < 0 || dev >= kNoAllocMaxDevices) return EVS_ERR_INVALID_ARG;
-    if (!g_noalloc_ptr[dev]) {
-        // one-time set-up on this device (the device is current here)
-        NoAllocScratch* p = nullptr;
-        if (cudaGetSymbolAddress((void**)&p, g_noalloc_scratch) != cudaSuccess || !p) return EVS_ERR_CUDA;
-        const int smem_max = gemm_tc_init();
-        if (smem_max < 0) return EVS_ERR_CUDA;
-        g_noalloc_smem[dev] = smem_max;
-        g_noalloc_ptr[dev] = p;
-    }
-    NoAllocScratch* sc = g_noalloc_ptr[dev];
-    // split-K partials always go through the fixed array here (no thread-block cluster)
-    TcShape t = tc_shape(M, N, K);
-    t.cluster = 0;
+    NoAllocScratch* sc = noalloc_scratch(s, &st, &dev);
+    if (!sc) return st;
+    // split-K partials always go through the fixed array here (no thread-block cluster);
+    // the split count is capped so that every partial tile fits it (one split always does)
+    const TcShape t = tc_shape(M, N, K, kNoAllocPartFloats, 1 << 30, /*allow_cluster=*/false);
     if (tc_part_floats(t, M, N) > kNoAllocPartFloats) return EVS_ERR_CAPACITY;
     CUtensorMap ta, tb;
     if (!make_map(&ta, W, (uint64_t)N, (uint64_t)K, TC_BM)) return EVS_ERR_CUDA;
     if (!make_map(&tb, X, (uint64_t)x_rows, (uint64_t)K, (uint32_t)(t.n_pad < 256 ? t.n_pad : 256))) return EVS_ERR_CUDA;
     if ((int)t.smem > g_noalloc_smem[dev]) return EVS_ERR_INVALID_ARG;
-    cudaStream_t s = (cudaStream_t)stream;
     // the array keeps the previous call's contents: the counters must start at zero
     if (cudaMemsetAsync(sc->counters, 0, sizeof(sc->counters), s) != cudaSuccess) return EVS_ERR_CUDA;
     TcArgs a{};
@@ -927,3 +947,19 @@ extern "C" evs_status evs_projection_noalloc(const void* X, int32_t x_rows, cons
     return cudaGetLastError() == cudaSuccess ? EVS_OK : EVS_ERR_CUDA;
 }
 
+extern "C" evs_status evs_projection_noalloc_flags(uint32_t* flags, int32_t clear, void* stream) {
+    using namespace evs;
+    if (!flags) return EVS_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    evs_status st = EVS_OK;
+    int dev = -1;
+    NoAllocScratch* sc = noalloc_scratch(s, &st, &dev);
+    if (!sc) return st;
+    uint32_t v = 0;
+    // a device-to-host copy into this stack word, then the stream is synchronised
+    if (cudaMemcpyAsync(&v, &sc->flags, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return EVS_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return EVS_ERR_CUDA;
+    *flags = v;
+    if (clear && cudaMemsetAsync(&sc->flags, 0, sizeof(uint32_t), s) != cudaSuccess) return EVS_ERR_CUDA;
+    return EVS_OK;
+}
