@@ -28,6 +28,7 @@ def _one_round(name, seqs, kv_dtype=np.float64):
     out = pair.run_round(gen_round(wl, 0), seqs=seqs)
     pair.compare_state_light(seqs, rows_from=wl.prefix_len)
     assert pair.ver.flags() == 0
+    assert pair.fp64_disagreements == 0, (out.gk, out.k, out.gc, out.corr, out.tie)
     return out
 
 

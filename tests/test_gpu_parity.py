@@ -25,9 +25,10 @@ def _build():
 
 def _lockstep(pair, rounds, first_round=0, drafts=None):
     """Run rounds on both sides; anchor = previous correction. Every round checks the
-    block outputs, the decisions in the kernel's precision and the sliced state. For fp32
-    workloads the oracle's own fp64 decisions must match too. Returns the number of rounds
-    the fp64 oracle flagged as near-ties."""
+    block outputs, the decisions in the kernel's precision and the sliced state. The
+    oracle's own fp64 decisions must match too (fp32 and bf16 alike), except on sequences
+    it flags as near-ties, which are counted. Returns the number of rounds with a flagged
+    near-tie."""
     ties = 0
     anchor = None
     for r in range(first_round, first_round + rounds):
@@ -37,11 +38,7 @@ def _lockstep(pair, rounds, first_round=0, drafts=None):
         out = pair.run_round(rnd)
         if out.tie.any():
             ties += 1
-        elif pair.wl.dtype == "f32":
-            np.testing.assert_array_equal(out.gk, out.k)
-            np.testing.assert_array_equal(out.gc, out.corr)
-            if pair.wl.n_cand > 1:
-                np.testing.assert_array_equal(out.gcand, out.cand)
+        assert pair.fp64_disagreements == 0, (r, out.gk, out.k, out.gc, out.corr, out.gcand, out.cand, out.tie)
         pair.compare_state()
         anchor = out.gc
     return ties
@@ -61,6 +58,63 @@ def identity_drafts(pair, rnd, wrong_at=None):
                     nxt = (nxt + 1) % pair.wl.vocab
                 toks[b, c, i + 1] = nxt
     return toks
+
+
+def identity_drafts_per_seq(pair, rnd, wrong_at):
+    """Drafts equal to the oracle's greedy chain, made wrong at draft wrong_at[b][c] + 1 of
+    sequence b, candidate c (None: every draft right), so that candidate accepts exactly
+    wrong_at[b][c] drafts (or gamma)."""
+    toks = rnd["tokens"].copy()
+    B, C, T = toks.shape
+    for b in range(B):
+        for c in range(C):
+            probe = pair.states[b].clone()
+            for i in range(T - 1):
+                nxt = int(np.argmax(pair.tgt.step(probe, int(toks[b, c, i]))))
+                if wrong_at[b][c] is not None and i == wrong_at[b][c]:
+                    nxt = (nxt + 1) % pair.wl.vocab
+                toks[b, c, i + 1] = nxt
+    return toks
+
+
+def _wide_geometry():
+    """The 4 x 4-candidate geometry at width 4096 (gamma 12, [FIR-3, IIR-16, FIR-7, attention
+    32 x 128]) in greedy mode with a short prefix."""
+    return get_workload("d4096_l8_p32k_b4c4_bf16").replace(
+        layers=(LayerSpec("fir", 3), LayerSpec("iir", 16), LayerSpec("fir", 7), LayerSpec("attn", 32)),
+        mode="greedy", prefix_len=96)
+
+
+@pytest.mark.parametrize("wrong_at,want_k,want_cand", [
+    # committed k = 1 (FIR-7 tail mixes 5 old-tail rows and 2 block rows), 5, 11, 12; the
+    # committed candidate is never candidate 0, so its K/V side rows are copied at k > 0
+    ([[0, 0, 1, 0], [1, 5, 3, 2], [0, 2, 4, 11], [3, None, None, 0]], [1, 5, 11, 12], [2, 1, 3, 1]),
+    # committed k = 0 (every candidate rejects its first draft), 6 (tail all block rows), 2, 12
+    ([[0, 0, 0, 0], [6, 0, 6, 1], [0, 1, 2, 0], [None, 11, 12 - 1, None]], [0, 6, 2, 12], [0, 0, 2, 0]),
+])
+def test_forced_slices_wide_multi_candidate(wrong_at, want_k, want_cand):
+    """State restoration at chosen block indices on the 4096-wide, gamma-12, 4 x 4-candidate
+    geometry (Figure 1(d): the block index k, the last L-1 FIR inputs, s_k): each sequence's
+    candidates accept the given numbers of drafts, the longest is committed, and the sliced
+    state (FIR-3 and FIR-7 tails, the IIR state rebuilt over k+1 steps, the committed
+    candidate's K/V rows, KV lengths) matches the oracle; one more round then runs from it."""
+    wl = _wide_geometry()
+    pair = Pair(wl)
+    pair.import_synthetic(wl.prefix_len)
+    rnd = gen_round(wl, 5)
+    rnd["tokens"] = identity_drafts_per_seq(pair, rnd, wrong_at)
+    kv0 = [s.kv_len for s in pair.states]
+    out = pair.run_round(rnd)
+    np.testing.assert_array_equal(out.k, want_k)          # the oracle's own fp64 decisions
+    np.testing.assert_array_equal(out.cand, want_cand)
+    for b in range(wl.batch):
+        if out.tie[b]:       # a flagged near-tie may flip the library's argmax: the oracle
+            continue         # then slices at the library's decision, compared below
+        assert (out.gk[b], out.gcand[b], out.gc[b]) == (want_k[b], want_cand[b], out.corr[b]), b
+    assert [s.kv_len for s in pair.states] == [k0 + int(k) + 1 for k0, k in zip(kv0, out.gk)]
+    pair.compare_state()
+    assert pair.ver.flags() == 0
+    _lockstep(pair, 1, first_round=6)
 
 
 def test_tiny_fp32_prefill_matches_oracle():
