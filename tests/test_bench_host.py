@@ -38,3 +38,32 @@ def test_round_bytes_min_counts_weights_kv_and_state():
     assert b > w + kv
     assert b < (w + kv) * 1.01                     # states and new rows are small beside them
     assert bench.kind_bytes(wl, P, "attn") == bench.kv_read_bytes(wl, P) == kv
+
+
+def test_oracle_sample_by_blocks_equals_verify_round():
+    """The CPU baseline takes a round one candidate block at a time; its decisions and the
+    committed state equal the oracle's whole-round call on the same inputs."""
+    import numpy as np
+    import bench
+    import oracle
+    from synth import gen_round, get_workload
+    wl = get_workload("tiny_d64_fp32").replace(batch=1, n_cand=3, gamma=4, mode="sampling", q_alpha=0.5,
+                                               prefix_len=40)
+    smp = bench.OracleSample(wl)
+    ref = [smp.state[0].clone()]
+    anchor = None
+    for r in range(4):
+        rnd = gen_round(smp.wl1, r, anchor=anchor)
+        want = oracle.verify_round(smp.tgt, ref, rnd["tokens"], rnd["q"], rnd["u"], wl.mode, wl.temperature,
+                                   rule=wl.cand_rule)
+        got = [smp.block() for _ in range(wl.n_cand)]
+        assert got[:-1] == [0] * (wl.n_cand - 1) and got[-1] == int(want.k[0]) + 1
+        assert smp.anchor[0] == want.corr[0]
+        anchor = want.corr
+        for a, b in zip(smp.state[0].layers, ref[0].layers):
+            if a["kind"] == "attn":
+                assert a["kv"].length == b["kv"].length
+                np.testing.assert_array_equal(a["kv"].k[:, :a["kv"].length], b["kv"].k[:, :b["kv"].length])
+            else:
+                key = "tail" if a["kind"] == "fir" else "s"
+                np.testing.assert_array_equal(a[key], b[key])
