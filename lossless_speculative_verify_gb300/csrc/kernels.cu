@@ -32,11 +32,34 @@ __global__ void embed_kernel(const T* __restrict__ E, const int32_t* __restrict_
     const T* row = E + (size_t)tok * d;
     float* out = h + (size_t)m * d;
     float ss = 0.f;
-    for (int c = threadIdx.x; c < d; c += blockDim.x) {
-        const float v = to_f32(row[c]);
-        out[c] = v;
-        ss += v * v;
-        if (hb) hb[(size_t)m * d + c] = __float2bfloat16_rn(v);
+    // eight consecutive channels a thread (d is a multiple of 64): 16- or 32-byte loads, two
+    // 16-byte stores of h and one of bf16(h)
+    for (int c = 8 * threadIdx.x; c < d; c += 8 * blockDim.x) {
+        float v[8];
+        if constexpr (sizeof(T) == 2) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(row + c);
+            const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 f = __bfloat1622float2(p2[k]);
+                v[2 * k] = f.x;
+                v[2 * k + 1] = f.y;
+            }
+        } else {
+            const float4 a = *reinterpret_cast<const float4*>(row + c), b4 = *reinterpret_cast<const float4*>(row + c + 4);
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b4.x; v[5] = b4.y; v[6] = b4.z; v[7] = b4.w;
+        }
+        *reinterpret_cast<float4*>(out + c) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4*>(out + c + 4) = make_float4(v[4], v[5], v[6], v[7]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ss += v[k] * v[k];
+        if (hb) {
+            uint4 pk;
+            __nv_bfloat162* q2 = reinterpret_cast<__nv_bfloat162*>(&pk);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) q2[k] = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+            *reinterpret_cast<uint4*>(hb + (size_t)m * d + c) = pk;
+        }
     }
     if (ssq) {  // the row's sum of squares in tile slot 0, the other slots cleared
         ss = block_sum(ss, red);
