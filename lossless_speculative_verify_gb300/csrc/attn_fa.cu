@@ -494,9 +494,10 @@ bool make_kv_map(CUtensorMap* m, const void* base, int t_max, int bh) {
 
 // Plan of a pass with Q (1..128) queries per sequence. Chunks first: the number of splits per
 // (sequence, head) that minimises waves of one CTA per SM x (tiles per CTA + 2), a CTA's
-// start-up and drain costing about two tiles' streaming. When that still takes five or more
-// waves, a persistent grid of FA_GRID CTAs over runs of tiles instead (each start-up paid
-// once per SM); each (sequence, head) then meets at most FA_GRID / H + 2 runs.
+// start-up and drain costing about two tiles' streaming. A persistent grid of FA_GRID CTAs
+// over runs of tiles (each start-up paid once per SM, about one Q restage per run) is taken
+// instead when its cost, tiles per SM + 3, is lower, or when the chunks take five or more
+// waves; each (sequence, head) then meets at most FA_GRID / H + 2 runs.
 AttnPlan attn_plan(int Q, int B, int H, int t_max, int smem_max) {
     AttnPlan p{};
     if (Q < 1 || Q > FA_ROWS || B > FA_MAX_B) return p;
@@ -513,7 +514,10 @@ AttnPlan attn_plan(int Q, int B, int H, int t_max, int smem_max) {
         if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = s; best_waves = waves; }
     }
     p.n_q = FA_ROWS;
-    if (best_waves >= 5) {
+    // the persistent grid: every SM streams an equal run of the key tiles of all (sequence,
+    // head) prefixes laid end to end; about one prefix boundary per run costs a Q restage
+    const long long runs_cost = (bh * total_tiles + FA_GRID - 1) / FA_GRID + 3;
+    if (best_waves >= 5 || runs_cost < best_cost) {
         p.runs = 1;
         p.splits = FA_GRID / H + 2;
     } else {
