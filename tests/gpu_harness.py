@@ -62,6 +62,7 @@ def wl_key(wl) -> str:
     """A name for a workload variant by its shape (tests replace fields of the named ones)."""
     kinds = "".join({"fir": "F", "iir": "I", "attn": "A"}[x.kind] + str(x.param) for x in wl.layers)
     return (f"d{wl.d}_{kinds}_b{wl.batch}c{wl.n_cand}_g{wl.gamma}_{wl.mode}_{wl.dtype}"
+            + (f"_v{wl.vocab}" if wl.vocab != 512 else "")
             + (f"_{wl.cand_rule}" if wl.n_cand > 1 and wl.mode == "sampling" else ""))
 
 

@@ -292,3 +292,29 @@ def test_device_flag_on_bad_token_and_bad_k():
     bad_k = torch.full((1,), 99, dtype=torch.int32, device="cuda")
     pair.ver.slice(bad_k)
     assert pair.ver.flags() & 2
+
+
+@pytest.mark.parametrize("vocab,gamma,mode", [(256, 6, "greedy"), (1024, 6, "sampling"), (2048, 31, "sampling"),
+                                              (4096, 12, "greedy"), (4096, 9, "sampling")])
+def test_vocabularies_and_largest_block_fp32(vocab, gamma, mode):
+    """Every instance of the acceptance kernel (1, 4, 8 and 16 token ids per thread; 2 is
+    the 512-entry vocabulary of the other cases) and the largest block, gamma 31 (32
+    positions), against the oracle over consecutive rounds with two candidates."""
+    wl = get_workload("tiny_d64_fp32").replace(vocab=vocab, gamma=gamma, mode=mode, batch=2, n_cand=2,
+                                               q_alpha=0.5)
+    pair = Pair(wl)
+    pair.import_synthetic(40)
+    _lockstep(pair, 3)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_rounds_from_the_empty_state(dtype):
+    """Verify rounds straight from the empty state: no cached keys, so each query attends
+    to the block's own keys only (the attention's prefix chunks are all empty)."""
+    if dtype == "f32":
+        wl = get_workload("tiny_d64_fp32").replace(prefix_len=0)
+    else:
+        wl = get_workload("d1024_l8_p8k_bf16").replace(d=256, head_dim=128, prefix_len=0, n_cand=2,
+            layers=(LayerSpec("fir", 3), LayerSpec("iir", 16), LayerSpec("fir", 7), LayerSpec("attn", 2)))
+    pair = Pair(wl)
+    assert _lockstep(pair, 3) <= 3
