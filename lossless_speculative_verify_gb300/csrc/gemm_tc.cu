@@ -857,7 +857,12 @@ bool launch_gemm_tc(evs_handle* h, const void* X, int x_rows, const void* W, flo
             did |= 2;
         }
     }
-    if (!launch_tc(t, ta, tb, a, h->stream, h->pdl != 0)) return false;
+    // The K/V-writing projection (an attention layer's QKV) starts once its predecessor has
+    // ended instead of beside it. Started early, its 96 three-CTA clusters (12288 wide) were
+    // placed piecemeal into the slots the predecessor freed, and the last one or two found no
+    // GPC with room until CTAs of the launch itself finished: a 15 us tail at 13 token rows.
+    const bool pdl = h->pdl != 0 && !(did & 2);
+    if (!launch_tc(t, ta, tb, a, h->stream, pdl)) return false;
     if (fused) *fused = did;
     return true;
 }
