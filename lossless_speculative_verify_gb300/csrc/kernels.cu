@@ -445,14 +445,16 @@ __global__ void __launch_bounds__(256) attn_split_kernel(
 // Merge the prefix partials with the in-block causal keys of the query's own candidate,
 // normalise, and store o in the projection dtype. One CTA (four warps) per (sequence x head,
 // candidate, four consecutive block positions), a warp per query; lanes own dh/32 output
-// columns. The partials are folded in eight chunks at a time (every load of a batch in
-// flight before any is used) with a running maximum; then the in-block keys j <= i, staged
+// columns. The partials are folded PB chunks at a time (every load of a batch in flight
+// before any is used) with a running maximum; then the in-block keys j <= i, staged
 // 32 rows at a time in shared memory, one score per lane, the same way. dh is 16..128.
 constexpr int CMB_ROWS = 32;
 constexpr int CMB_DHMAX = 128;
 
-template <typename T, int EPL>
-__global__ void __launch_bounds__(128, 4) attn_combine_kernel(
+// PB = 4 leaves registers for five bf16 CTAs an SM, for grids of several waves; PB = 8 takes
+// one round trip fewer where five or six chunks meet a query.
+template <typename T, int EPL, int PB>
+__global__ void __launch_bounds__(128, (PB == 4 && sizeof(T) == 2) ? 5 : 4) attn_combine_kernel(
     const float* __restrict__ Y, int ldy, const T* __restrict__ kc, const T* __restrict__ vc,
     const T* __restrict__ ks, const T* __restrict__ vs, int H, int dh, int C, int Tb, int Q, int q_max,
     int t_max, int splits, int chunk, int B, int fa_grid, int in_cache, const int32_t* __restrict__ kv_base,
@@ -553,10 +555,10 @@ __global__ void __launch_bounds__(128, 4) attn_combine_kernel(
     if (live) {
         const float* pq = part + ((size_t)bh * splits * q_max + qi) * (dh + 2);
         const size_t pstride = (size_t)q_max * (dh + 2);
-        for (int s0 = 0; s0 < used; s0 += 8) {
-            float ms[8], ls[8], os[8][EPL];
+        for (int s0 = 0; s0 < used; s0 += PB) {
+            float ms[PB], ls[PB], os[PB][EPL];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < PB; ++j) {
                 const bool on = s0 + j < used;
                 ms[j] = on ? pq[(s0 + j) * pstride + dh] : -INFINITY;
                 ls[j] = on ? pq[(s0 + j) * pstride + dh + 1] : 0.f;
@@ -565,11 +567,11 @@ __global__ void __launch_bounds__(128, 4) attn_combine_kernel(
             }
             float mb = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) mb = fmaxf(mb, ms[j]);
+            for (int j = 0; j < PB; ++j) mb = fmaxf(mb, ms[j]);
             if (mb == -INFINITY) continue;        // empty chunks only
             rebase(mb);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < PB; ++j) {
                 if (ms[j] == -INFINITY) continue;  // an empty chunk leaves its o unwritten
                 const float w = __expf(ms[j] - M);
                 L = fmaf(ls[j], w, L);
@@ -1220,10 +1222,21 @@ void launch_attention(evs_handle* h, int li, const Pass& p) {
     prof_end(h, EVS_K_ATTN);
     prof_begin(h, EVS_K_ATTN_COMBINE);
     dim3 grid2(p.B * H, p.C, (p.T + 3) / 4);
-#define EVS_CMB(TY, EPL)                                                                                \
-    launch_k(h, attn_combine_kernel<TY, EPL>, dim3(grid2), dim3(128), 0, h->y, 3 * d, (const TY*)L.kc,       \
-             (const TY*)L.vc, (const TY*)L.ks, (const TY*)L.vs, H, dh, p.C, p.T, Q, g.q_max, h->cfg.t_max, \
-             splits, chunk, p.B, fa_grid, p.kv_in_cache, h->kv_base, h->attn_part, (TY*)h->act, d)
+    // more CTAs than one wave at four an SM: the smaller batch, for a fifth CTA an SM
+    const bool waves = (long long)grid2.x * grid2.y * grid2.z > 4LL * kAttnGrid;
+#define EVS_CMB(TY, EPL)                                                                                    \
+    do {                                                                                                    \
+        if (waves)                                                                                          \
+            launch_k(h, attn_combine_kernel<TY, EPL, 4>, dim3(grid2), dim3(128), 0, h->y, 3 * d,            \
+                     (const TY*)L.kc, (const TY*)L.vc, (const TY*)L.ks, (const TY*)L.vs, H, dh, p.C, p.T, Q, \
+                     g.q_max, h->cfg.t_max, splits, chunk, p.B, fa_grid, p.kv_in_cache, h->kv_base,        \
+                     h->attn_part, (TY*)h->act, d);                                                         \
+        else                                                                                                \
+            launch_k(h, attn_combine_kernel<TY, EPL, 8>, dim3(grid2), dim3(128), 0, h->y, 3 * d,            \
+                     (const TY*)L.kc, (const TY*)L.vc, (const TY*)L.ks, (const TY*)L.vs, H, dh, p.C, p.T, Q, \
+                     g.q_max, h->cfg.t_max, splits, chunk, p.B, fa_grid, p.kv_in_cache, h->kv_base,        \
+                     h->attn_part, (TY*)h->act, d);                                                         \
+    } while (0)
     if (is_bf16(h)) {
         if (dh > 64) EVS_CMB(bf16, 4); else if (dh > 32) EVS_CMB(bf16, 2); else EVS_CMB(bf16, 1);
     } else {
