@@ -244,12 +244,13 @@ __global__ void __launch_bounds__(256) iir_kernel(const float* __restrict__ Y, i
 }
 
 // The same scan with four poles per thread (N/4 lanes per channel): the readout needs only
-// log2(N/4) shuffle levels.
+// log2(N/4) shuffle levels. With 16 bf16 poles, four CTAs an SM (64 registers, no spills): 1024
+// CTAs at 4 x 4 candidates take 1.7 waves instead of 2.2 (-1.7 us per round).
 template <typename T, int NP>
-__global__ void __launch_bounds__(256) iir_quad_kernel(const float* __restrict__ Y, int ldy, T* __restrict__ out,
-                                                       int d, int C, int Tb, int commit,
-                                                       const float2* __restrict__ lam, const float2* __restrict__ bb,
-                                                       const float2* __restrict__ cc, float2* __restrict__ state) {
+__global__ void __launch_bounds__(256, (NP == 16 && sizeof(T) == 2) ? 4 : 2)
+    iir_quad_kernel(const float* __restrict__ Y, int ldy, T* __restrict__ out, int d, int C, int Tb, int commit,
+                    const float2* __restrict__ lam, const float2* __restrict__ bb, const float2* __restrict__ cc,
+                    float2* __restrict__ state) {
     constexpr int PPT = NP < 4 ? NP : 4;     // poles per thread
     constexpr int LPC = NP / PPT;            // lanes per channel
     pdl_trigger();
