@@ -94,6 +94,18 @@ struct TcArgs {
     __nv_bfloat16* vs;
 };
 
+// The epilogue a launch runs, fixed at compile time: each instantiation carries only its own
+// epilogue code, which runs once per CTA from a cold instruction cache (instruction-fetch
+// stalls were a fifth of the stall cycles of the single kernel with every epilogue).
+enum TcEpi : int {
+    TC_EPI_PLAIN = 0,     // no split-K: TMEM straight to the outputs
+    TC_EPI_CLUSTER = 1,   // split-K reduced by row runs within the cluster
+    TC_EPI_GLOBAL = 2,    // split-K reduced by the last CTA of a tile
+    TC_EPI_FIR = 3,       // in-projection with the FIR mixer
+    TC_EPI_IIR = 4,       // in-projection with the modal IIR mixer
+};
+
+template <int EPI>
 __global__ void __launch_bounds__(128, 2)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcArgs p) {
     extern __shared__ uint8_t smem_raw[];
@@ -244,9 +256,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     };
     float fw[16];
     float2 il[4], ib[4], ic[4], is[4];
-    if (p.mix == 1) {
+    if constexpr (EPI == TC_EPI_FIR) {
         fir_load(threadIdx.x, fw);
-    } else if (p.mix == 2) {
+    } else if constexpr (EPI == TC_EPI_IIR) {
         iir_load(threadIdx.x, il, ib, ic, is);
     }
     if (p.ssq_in && warp >= 2) {
@@ -384,7 +396,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     int own_lo = 0, own_hi = 0;   // token rows whose sums of squares this CTA completes
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
     const int nl_lane = warp * 32 + lane;
-    if (p.mix) {
+    if constexpr (EPI == TC_EPI_FIR || EPI == TC_EPI_IIR) {
         // ---- in-projection + mixer: gather this CTA's channel slice of v for every token
         // row (whole tile without split-K; a 1/S share of the channels with a cluster), then
         // one thread per (sequence-candidate, channel) runs the FIR / modal IIR over time
@@ -433,7 +445,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         auto xin = [&](int g, int t, int c) -> float {
             return vals[(size_t)(g * T + t) * vld + voff + c] * (p.ssq_in ? rinv_s[g * T + t] : 1.f);
         };
-        if (p.mix == 1) {
+        if constexpr (EPI == TC_EPI_FIR) {
             // FIR, y_t = sum_j w_j x_{t-j}: no recurrence, so one thread per (group, block
             // position, channel), channels fastest (coalesced stores); x_{-m} for m >= 1 is
             // row L-1-m of the carried tail
@@ -496,7 +508,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     __syncthreads();
                 }
             }
-        } else if (p.mix == 2) {
+        } else {
             // modal IIR: a thread per (group, channel, quad of four poles); the readout of
             // eight positions at a time is reduced over the channel's N/4 lanes side by side.
             // A verify pass keeps the inputs u_t (slicing recomputes s_k from them).
@@ -542,7 +554,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
             }
         }
-    } else if (p.splits == 1) {
+    } else if constexpr (EPI == TC_EPI_PLAIN) {
         for (int c0 = 0; c0 < p.M; c0 += 16) {
             float v[16], r[16];
 #pragma unroll
@@ -553,7 +565,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 if (c0 + j < p.M) finish(c0 + j, nl_lane, v[j], r[j], !bad);
         }
         own_hi = p.M;
-    } else if (p.cluster) {
+    } else if constexpr (EPI == TC_EPI_CLUSTER) {
         // split-K within the cluster through L2: every rank stores its partial tile to the
         // scratch, one cluster barrier, then each rank adds a run of rows over the ranks in
         // rank order (deterministic) and finishes them: a row per warp, four channels a lane
@@ -673,16 +685,32 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
 
 // Opt the kernel into the largest dynamic shared memory the device allows next to its
 // static shared memory; returns that size in bytes, or -1 on failure.
+using TcKernel = void (*)(const CUtensorMap, const CUtensorMap, TcArgs);
+static const TcKernel kTcKernels[] = {gemm_tc_kernel<TC_EPI_PLAIN>, gemm_tc_kernel<TC_EPI_CLUSTER>,
+                                      gemm_tc_kernel<TC_EPI_GLOBAL>, gemm_tc_kernel<TC_EPI_FIR>,
+                                      gemm_tc_kernel<TC_EPI_IIR>};
+
+// The instantiation for a launch's arguments.
+static TcKernel tc_kernel_for(const TcArgs& a) {
+    if (a.mix == 1) return kTcKernels[TC_EPI_FIR];
+    if (a.mix == 2) return kTcKernels[TC_EPI_IIR];
+    if (a.splits == 1) return kTcKernels[TC_EPI_PLAIN];
+    return kTcKernels[a.cluster ? TC_EPI_CLUSTER : TC_EPI_GLOBAL];
+}
+
 int gemm_tc_init() {
     int dev = 0, optin = 0;
-    cudaFuncAttributes fa;
     if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-        cudaFuncGetAttributes(&fa, gemm_tc_kernel) != cudaSuccess)
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return -1;
-    const int dyn = optin - (int)fa.sharedSizeBytes;
-    if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn) != cudaSuccess)
-        return -1;
+    int dyn = optin;
+    for (TcKernel k : kTcKernels) {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, k) != cudaSuccess) return -1;
+        dyn = std::min(dyn, optin - (int)fa.sharedSizeBytes);
+    }
+    for (TcKernel k : kTcKernels)
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn) != cudaSuccess) return -1;
     return dyn;
 }
 
@@ -773,7 +801,7 @@ static bool launch_tc(const TcShape& t, const CUtensorMap& ta, const CUtensorMap
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, ta, tb, a) == cudaSuccess;
+    return cudaLaunchKernelEx(&cfg, tc_kernel_for(a), ta, tb, a) == cudaSuccess;
 }
 
 bool gemm_tc_supported(int M, int N, int K) {
