@@ -105,7 +105,8 @@ enum TcEpi : int {
     TC_EPI_IIR = 4,       // in-projection with the modal IIR mixer
 };
 
-template <int EPI>
+// KV: the launch writes K / V columns to the cache or side buffer (an attention layer's QKV).
+template <int EPI, bool KV>
 __global__ void __launch_bounds__(128, 2)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcArgs p) {
     extern __shared__ uint8_t smem_raw[];
@@ -291,10 +292,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // share added per thread), -1 past the end of the cache. Shares red_s with the sums of
     // squares, which a K/V-writing launch never produces.
     long long* kv_row = reinterpret_cast<long long*>(red_s);
-    const bool kv_ch = p.kv && n0 + (int)threadIdx.x >= p.d;   // this thread's channel is K or V
+    const bool kv_ch = KV && n0 + (int)threadIdx.x >= p.d;   // this thread's channel is K or V
     long long kv_col = 0;
     __nv_bfloat16* kv_dst = nullptr;
-    if (p.kv) {
+    if constexpr (KV) {
         for (int m = threadIdx.x; m < p.M; m += blockDim.x) {
             const int bc = m / p.kv_T, i = m % p.kv_T, b = bc / p.kv_C;
             long long o;
@@ -686,16 +687,19 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
 // Opt the kernel into the largest dynamic shared memory the device allows next to its
 // static shared memory; returns that size in bytes, or -1 on failure.
 using TcKernel = void (*)(const CUtensorMap, const CUtensorMap, TcArgs);
-static const TcKernel kTcKernels[] = {gemm_tc_kernel<TC_EPI_PLAIN>, gemm_tc_kernel<TC_EPI_CLUSTER>,
-                                      gemm_tc_kernel<TC_EPI_GLOBAL>, gemm_tc_kernel<TC_EPI_FIR>,
-                                      gemm_tc_kernel<TC_EPI_IIR>};
+// [KV][epilogue]; the mixers never write K / V
+static const TcKernel kTcKernels[2][5] = {
+    {gemm_tc_kernel<TC_EPI_PLAIN, false>, gemm_tc_kernel<TC_EPI_CLUSTER, false>,
+     gemm_tc_kernel<TC_EPI_GLOBAL, false>, gemm_tc_kernel<TC_EPI_FIR, false>, gemm_tc_kernel<TC_EPI_IIR, false>},
+    {gemm_tc_kernel<TC_EPI_PLAIN, true>, gemm_tc_kernel<TC_EPI_CLUSTER, true>,
+     gemm_tc_kernel<TC_EPI_GLOBAL, true>, nullptr, nullptr}};
 
 // The instantiation for a launch's arguments.
 static TcKernel tc_kernel_for(const TcArgs& a) {
-    if (a.mix == 1) return kTcKernels[TC_EPI_FIR];
-    if (a.mix == 2) return kTcKernels[TC_EPI_IIR];
-    if (a.splits == 1) return kTcKernels[TC_EPI_PLAIN];
-    return kTcKernels[a.cluster ? TC_EPI_CLUSTER : TC_EPI_GLOBAL];
+    if (a.mix == 1) return kTcKernels[0][TC_EPI_FIR];
+    if (a.mix == 2) return kTcKernels[0][TC_EPI_IIR];
+    const int e = a.splits == 1 ? TC_EPI_PLAIN : (a.cluster ? TC_EPI_CLUSTER : TC_EPI_GLOBAL);
+    return kTcKernels[a.kv ? 1 : 0][e];
 }
 
 int gemm_tc_init() {
@@ -704,13 +708,16 @@ int gemm_tc_init() {
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return -1;
     int dyn = optin;
-    for (TcKernel k : kTcKernels) {
-        cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, k) != cudaSuccess) return -1;
-        dyn = std::min(dyn, optin - (int)fa.sharedSizeBytes);
-    }
-    for (TcKernel k : kTcKernels)
-        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn) != cudaSuccess) return -1;
+    for (const auto& row : kTcKernels)
+        for (TcKernel k : row) {
+            cudaFuncAttributes fa;
+            if (k && cudaFuncGetAttributes(&fa, k) != cudaSuccess) return -1;
+            if (k) dyn = std::min(dyn, optin - (int)fa.sharedSizeBytes);
+        }
+    for (const auto& row : kTcKernels)
+        for (TcKernel k : row)
+            if (k && cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn) != cudaSuccess)
+                return -1;
     return dyn;
 }
 
