@@ -106,7 +106,9 @@ enum TcEpi : int {
 };
 
 // KV: the launch writes K / V columns to the cache or side buffer (an attention layer's QKV).
-template <int EPI, bool KV>
+// FL: the FIR mixer's filter length when fixed at compile time (0: up to 16, from the
+// arguments), so that its once-per-CTA code holds only the taps it has.
+template <int EPI, bool KV, int FL = 0>
 __global__ void __launch_bounds__(128, 2)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcArgs p) {
     extern __shared__ uint8_t smem_raw[];
@@ -233,12 +235,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int mT = p.mix_T > 0 ? p.mix_T : 1, mgroups = p.M / mT;
     // FIR item: one (group g, block position t, channel c), channels fastest: its taps w[j],
     // zero past the filter length
-    auto fir_load = [&](int item, float (&w)[16]) {
-        const int L = p.mix_param;
+    constexpr int KL = FL > 0 ? FL : 16;   // FIR taps held per item
+    auto fir_load = [&](int item, float (&w)[KL]) {
+        const int L = FL > 0 ? FL : p.mix_param;
         const bool on = item < mgroups * mT * mcw;
         const int n = n0 + mc_lo + (on ? item % mcw : 0);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) w[j] = (on && j < L) ? p.taps[(size_t)n * L + j] : 0.f;
+        for (int j = 0; j < KL; ++j) w[j] = (on && j < L) ? p.taps[(size_t)n * L + j] : 0.f;
     };
     // IIR item: one (g, channel, quad of four poles); pole lambda, input weight B, readout
     // weight C and carried state of the quad's poles
@@ -255,7 +258,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             sv[k] = on ? p.state[((size_t)b * p.d + n) * N + k0 + k] : make_float2(0.f, 0.f);
         }
     };
-    float fw[16];
+    float fw[KL];
     float2 il[4], ib[4], ic[4], is[4];
     if constexpr (EPI == TC_EPI_FIR) {
         fir_load(threadIdx.x, fw);
@@ -450,31 +453,31 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // FIR, y_t = sum_j w_j x_{t-j}: no recurrence, so one thread per (group, block
             // position, channel), channels fastest (coalesced stores); x_{-m} for m >= 1 is
             // row L-1-m of the carried tail
-            const int L = p.mix_param;
+            const int L = FL > 0 ? FL : p.mix_param;
             const int items = groups * T * cw;
             for (int it = threadIdx.x; it < items && !bad; it += blockDim.x) {
                 if (it != (int)threadIdx.x && blockDim.x % cw != 0) fir_load(it, fw);   // else same channel
                 const int c = it % cw, t = (it / cw) % T, g = it / (cw * T);
                 const int n = n0 + c_lo + c, b = g / p.mix_C;
                 const float* tl = p.tail + (size_t)b * (L - 1) * p.d + n;
-                float xv[16];   // x_{t-j}: every input's load issued before the sum
+                float xv[KL];   // x_{t-j}: every input's load issued before the sum
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
+                for (int j = 0; j < KL; ++j)
                     xv[j] = j >= L ? 0.f : (t - j >= 0 ? xin(g, t - j, c) : tl[(size_t)(L - 1 - j + t) * p.d]);
                 float y = fw[0] * xv[0];
 #pragma unroll
-                for (int j = 1; j < 16; ++j)
+                for (int j = 1; j < KL; ++j)
                     if (j < L) y = fmaf(fw[j], xv[j], y);
                 p.mix_out[((size_t)g * T + t) * p.d + n] = __float2bfloat16_rn(y);
                 if (!p.mix_commit) {   // stage rows [tail || block inputs] of this group
                     float* st = p.stage + (size_t)g * (L - 1 + T) * p.d + n;
                     st[(size_t)(L - 1 + t) * p.d] = xv[0];
                     if (t == 0) {   // every row's load issued before any store
-                        float tv[15];
+                        float tv[KL];
 #pragma unroll
-                        for (int r = 0; r < 15; ++r) tv[r] = r < L - 1 ? tl[(size_t)r * p.d] : 0.f;
+                        for (int r = 0; r < KL - 1; ++r) tv[r] = r < L - 1 ? tl[(size_t)r * p.d] : 0.f;
 #pragma unroll
-                        for (int r = 0; r < 15; ++r)
+                        for (int r = 0; r < KL - 1; ++r)
                             if (r < L - 1) st[(size_t)r * p.d] = tv[r];
                     }
                 }
@@ -694,9 +697,13 @@ static const TcKernel kTcKernels[2][5] = {
     {gemm_tc_kernel<TC_EPI_PLAIN, true>, gemm_tc_kernel<TC_EPI_CLUSTER, true>,
      gemm_tc_kernel<TC_EPI_GLOBAL, true>, nullptr, nullptr}};
 
+// FIR mixers of the filter lengths the layers use, fixed at compile time
+static const TcKernel kTcFir3 = gemm_tc_kernel<TC_EPI_FIR, false, 3>;
+static const TcKernel kTcFir7 = gemm_tc_kernel<TC_EPI_FIR, false, 7>;
+
 // The instantiation for a launch's arguments.
 static TcKernel tc_kernel_for(const TcArgs& a) {
-    if (a.mix == 1) return kTcKernels[0][TC_EPI_FIR];
+    if (a.mix == 1) return a.mix_param == 3 ? kTcFir3 : a.mix_param == 7 ? kTcFir7 : kTcKernels[0][TC_EPI_FIR];
     if (a.mix == 2) return kTcKernels[0][TC_EPI_IIR];
     const int e = a.splits == 1 ? TC_EPI_PLAIN : (a.cluster ? TC_EPI_CLUSTER : TC_EPI_GLOBAL);
     return kTcKernels[a.kv ? 1 : 0][e];
@@ -707,17 +714,21 @@ int gemm_tc_init() {
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return -1;
-    int dyn = optin;
-    for (const auto& row : kTcKernels)
-        for (TcKernel k : row) {
-            cudaFuncAttributes fa;
-            if (k && cudaFuncGetAttributes(&fa, k) != cudaSuccess) return -1;
-            if (k) dyn = std::min(dyn, optin - (int)fa.sharedSizeBytes);
-        }
+    TcKernel all[12];
+    int n = 0;
     for (const auto& row : kTcKernels)
         for (TcKernel k : row)
-            if (k && cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn) != cudaSuccess)
-                return -1;
+            if (k) all[n++] = k;
+    all[n++] = kTcFir3;
+    all[n++] = kTcFir7;
+    int dyn = optin;
+    for (int i = 0; i < n; ++i) {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, all[i]) != cudaSuccess) return -1;
+        dyn = std::min(dyn, optin - (int)fa.sharedSizeBytes);
+    }
+    for (int i = 0; i < n; ++i)
+        if (cudaFuncSetAttribute(all[i], cudaFuncAttributeMaxDynamicSharedMemorySize, dyn) != cudaSuccess) return -1;
     return dyn;
 }
 
