@@ -235,6 +235,19 @@ def test_multi_candidate_bf16_wide_block():
     _lockstep(pair, 3)
 
 
+@pytest.mark.parametrize("batch,n_cand", [(1, 1), (4, 4)], ids=["fused_mixers", "standalone_scans"])
+def test_bf16_other_filter_lengths_and_poles(batch, n_cand):
+    """FIR lengths 5 and 16 and an 8-pole IIR: the projection's generic FIR epilogue (the
+    lengths 3 and 7 have instantiations of their own) and the modal scan at another pole
+    count, fused in the in-projections at 7 rows and standalone at 112 rows."""
+    wl = get_workload("tiny_d64_fp32").replace(
+        d=256, dtype="bf16", head_dim=128, batch=batch, n_cand=n_cand, gamma=6, mode="sampling",
+        layers=(LayerSpec("fir", 5), LayerSpec("iir", 8), LayerSpec("fir", 16), LayerSpec("attn", 2)))
+    pair = Pair(wl)
+    pair.import_synthetic(150)
+    _lockstep(pair, 3)
+
+
 def test_bf16_small_stack_sampling():
     wl = get_workload("d1024_l8_p8k_bf16").replace(d=256, head_dim=128, prefix_len=500,
         layers=(LayerSpec("fir", 3), LayerSpec("iir", 16), LayerSpec("fir", 3), LayerSpec("attn", 2)) * 2)
